@@ -1,0 +1,322 @@
+"""Decode benchmark of the persistent megakernel (one JSON line on stdout).
+
+Default workload: the Llama-3-8B-shaped decoder at batch 1 — a 39-token
+random prompt followed by greedy decode steps, the single-GPU decode setting
+the MPK pages measure (16 GB of weights, 39-token prompt, 512 generated
+tokens).  A "step" is one decode step of the whole hot path (embedding,
+32 x [RMSNorm+QKV+RoPE, attention with KV append, O+residual,
+RMSNorm+gate/up+SiLU*mul, down+residual], final RMSNorm + LM head) plus the
+device-side greedy pick of the next token.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mk|reference]
+
+With N > 1 (torchrun) every rank runs an independent replica on its own GPU
+(the decode step has no exchange step to shard); the barrier + max over
+ranks brackets the timed region.  --impl reference times the fp64 CPU
+oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from dataclasses import replace
+from pathlib import Path
+
+import numpy as np
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+import synth  # noqa: E402
+from synth import WORKLOADS  # noqa: E402
+
+METRIC = "decode ms/token (batch 1) + achieved HBM GB/s vs B300 peak per step"
+FALLBACK_HBM_GBS = 6400.0
+
+
+def step_bytes(m, batch: int, ctx: int) -> int:
+    """Algorithmic HBM bytes of one decode step at context length ctx (the new
+    token included): every weight once, every cached K/V entry once, the new
+    K/V entry written once, the logits written once."""
+    per_tok = 2 * m.n_layers * m.n_kv_heads * m.head_dim * 2  # K and V, all layers, bf16
+    return synth.weight_bytes(m) + batch * (per_tok * (ctx - 1) + per_tok + m.vocab * 4)
+
+
+def measured_peak():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        return float(json.loads(p.read_text())["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [v for v in (num(r[1]) for r in self.rows) if v is not None]
+        mx = [v for v in (num(r[2]) for r in self.rows) if v is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in self.rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows),
+                "power_w_max": max((num(r[3]) or 0.0) for r in self.rows)}
+
+
+# ----------------------------------------------------------------- CPU side
+
+def oracle_sample(m, steps: int, pos0: int, seed: int = 0, n_layers_gen: int = 2):
+    """Times the fp64 oracle, as it stands, on a bounded sample of the decode
+    step: each sample is ONE decoder layer (cycling over n_layers_gen
+    generated layers) plus 1/n_layers of the LM-head rows, so n_layers
+    samples cost one whole token.  Returns (ms per token, threads, text)."""
+    import oracle
+
+    layers = [synth.host_layer_weights(m, seed, l) for l in range(n_layers_gen)]
+    rows = max(1, m.vocab // m.n_layers)
+    head = synth.normal_bf16((rows, m.hidden), seed, synth.TID_LM_HEAD, m.weight_std)
+    fin = synth.normal_bf16((m.hidden,), seed, synth.TID_FINAL_NORM, 0.0, 1.0)
+    emb = synth.normal_bf16((1, m.hidden), seed, synth.TID_EMBED, m.weight_std)
+    model = oracle.Model(replace(m, vocab=rows), {"embed": emb, "lm_head": head, "final_norm": fin})
+    max_seq = pos0 + steps + 1
+    kc = np.zeros((max_seq, m.n_kv_heads, m.head_dim))
+    vc = np.zeros_like(kc)
+    x = model.embed_token(0)
+    times = []
+    for i in range(steps):
+        t0 = time.perf_counter()
+        model.layer_step(layers[i % n_layers_gen], kc, vc, pos0 + i, x)
+        model.head(x)
+        times.append(time.perf_counter() - t0)
+    per_token_ms = 1e3 * statistics.mean(times) * m.n_layers
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    desc = (f"{steps} samples of one {m.name} decoder layer + 1/{m.n_layers} of the LM-head rows at positions "
+            f"{pos0}..{pos0 + steps - 1}, fp64 oracle, scaled x{m.n_layers} to one token")
+    return per_token_ms, threads, desc
+
+
+def run_reference(args, wl):
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    m = wl.model
+    oracle_sample(m, args.warmup, wl.prompt_len)
+    ms, threads, desc = oracle_sample(m, args.steps, wl.prompt_len)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": ms, "unit": "ms/token", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded random-init weights)",
+        "config": {"workload": args.workload, "model": m.name, "batch": wl.batch, "prompt_len": wl.prompt_len},
+        "cpu_baseline": {"value": ms, "unit": "ms/token", "cores": threads, "kind": "oracle", "sample": desc},
+        "e2e": {"value": ms, "unit": "ms/token", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- GPU side
+
+def run_mk(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    import persistent_decode_megakernel_04_b300 as mk
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    m = wl.model
+    B = wl.batch
+    max_seq = ((wl.prompt_len + args.warmup + args.steps + args.e2e_steps + 4 + 63) // 64) * 64
+    weights = synth.device_weights(m, wl.seed, device=dev)
+    plan = mk.Plan(m, weights, batch=B, max_seq=max_seq)
+    kv = mk.KVCache(m, B, max_seq, shuffle_seed=1, device=dev)
+    prompt = np.stack([synth.tokens(wl.prompt_len, wl.seed, b, m.vocab) for b in range(B)])
+    toks = torch.tensor(prompt, dtype=torch.int32, device=dev)
+    logits = torch.empty((B, m.vocab), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    plan.prefill(toks, kv, logits)
+    tok = torch.empty(B, dtype=torch.int32, device=dev)
+    pos = torch.full((B,), wl.prompt_len - 1, dtype=torch.int32, device=dev)
+    plan.greedy_next(logits, tok, pos)  # first generated token, at position prompt_len
+    for _ in range(args.warmup):
+        plan.decode_step(tok, pos, kv, logits)
+        plan.greedy_next(logits, tok, pos)
+    plan.check()
+    ctx0 = wl.prompt_len + args.warmup + 1  # context length (new token included) of the first timed step
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        time.sleep(0.3)
+        start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            plan.decode_step(tok, pos, kv, logits)
+            ev[i][1].record(stream)
+            plan.greedy_next(logits, tok, pos)
+        end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    plan.check()
+    ms_step = start.elapsed_time(end) / args.steps
+    kern_ms = [a.elapsed_time(b) for a, b in ev]
+    if world > 1:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    bytes_total = sum(step_bytes(m, B, ctx0 + i) for i in range(args.steps))
+    achieved = bytes_total / (sum(kern_ms) / 1e3) / 1e9
+    peak, peak_src = measured_peak()
+    clk = clocks.summary()
+
+    # end to end through the host-buffer entry point: token in, logits out, host argmax
+    h_tok = torch.empty(B, dtype=torch.int32).pin_memory()
+    h_pos = torch.empty(B, dtype=torch.int32).pin_memory()
+    h_log = torch.empty((B, m.vocab), dtype=torch.float32).pin_memory()
+    h_tok.copy_(tok.cpu())
+    h_pos.copy_(pos.cpu())
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        plan.decode_step_host(h_tok, h_pos, kv, h_log)
+        h_tok.copy_(torch.argmax(h_log, dim=1).to(torch.int32))
+        h_pos += 1
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.e2e_steps
+
+    # launch-per-operator ablation of the same task code
+    abl = {}
+    if args.ablation_steps:
+        pos_a, tok_a = h_pos.to(dev), h_tok.to(dev)
+        for _ in range(2):
+            plan.decode_step_ablation(tok_a, pos_a, kv, logits)
+        torch.cuda.synchronize()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(args.ablation_steps):
+            plan.decode_step_ablation(tok_a, pos_a, kv, logits)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        abl["launch_per_op_ms_per_step"] = s0.elapsed_time(s1) / args.ablation_steps
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            plan.decode_step_ablation(tok_a, pos_a, kv, logits)
+        g.replay()
+        torch.cuda.synchronize()
+        s0.record(stream)
+        for _ in range(args.ablation_steps):
+            g.replay()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        abl["launch_per_op_graph_ms_per_step"] = s0.elapsed_time(s1) / args.ablation_steps
+        abl["launches_per_step"] = 5 * m.n_layers + 1
+        abl["ctx"] = int(pos_a[0].item()) + 1
+        plan.check()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        ms, threads, desc = oracle_sample(m, args.cpu_samples, wl.prompt_len)
+        cpu = {"value": ms, "unit": "ms/token", "cores": threads, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": ms_step / B, "unit": "ms/token", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16 weights/KV, fp32 math",
+            "data": "synthetic (seeded random-init weights, random prompt ids)",
+            "config": {"workload": args.workload, "model": m.name, "batch": B, "prompt_len": wl.prompt_len,
+                       "ctx_first_timed": ctx0, "ctx_last_timed": ctx0 + args.steps - 1,
+                       "parallelism": f"replicas x{world}",
+                       "l2": "no flush: ~15 GB of weights stream per step (> 126 MB L2)"},
+            "tokens_per_s": 1e3 / ms_step * B * world,
+            "hbm_gbs": achieved,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": peak_src, "traffic": None,
+                         "kernel": "megakernel", "kernel_ms_mean": statistics.mean(kern_ms),
+                         "bytes_per_step_mean": bytes_total / args.steps},
+            "clocks": clk,
+            "e2e": {"value": e2e_ms / B, "unit": "ms/token", "h2d_bytes_per_step": 8 * B,
+                    "d2h_bytes_per_step": 4 * B * m.vocab},
+            "gpu_launches": 2 * args.steps,
+            "ablation": abl,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    plan.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["mk", "reference"], default="mk")
+    ap.add_argument("--workload", default="8b", choices=sorted(WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=32)
+    ap.add_argument("--ablation-steps", type=int, default=8)
+    ap.add_argument("--cpu-samples", type=int, default=16)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    wl = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_mk(args, wl)
+
+
+if __name__ == "__main__":
+    main()

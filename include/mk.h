@@ -1,0 +1,195 @@
+/*
+ * mk.h — C ABI of the persistent decode megakernel for B300 (sm_103a).
+ *
+ * One decode step of a Llama-style decoder (RMSNorm, QKV projection, RoPE,
+ * GQA attention over a paged bf16 KV cache, O-projection + residual, SwiGLU
+ * MLP, LM head) runs as ONE cooperative kernel launch.  Inside it, every SM
+ * hosts one worker CTA with a scheduler warp, a weight-streaming producer
+ * warp and eight compute warps; tasks are ordered by global-memory event
+ * counters, never by kernel boundaries or grid-wide barriers.
+ *
+ * Where each operation is defined (page titles and sections):
+ *  - single-kernel execution of the whole step, task graph of per-SM tasks
+ *    and events, worker loop, scheduler warps, counter-with-threshold events:
+ *    "Compilar LLM en un MegaKernel para lograr inferencia de baja latencia"
+ *    (es.news.hada.io/topic?id=21563), sections "Parte 1. Compilador",
+ *    "Parte 2. Runtime", "Método de ejecución basado en eventos";
+ *  - the tGraph of SM-level tasks, ahead-of-time task preparation and the
+ *    paged shared memory that lets the next task's data load while the
+ *    current one finishes: "MPK: A Compiler and Runtime for Mega-Kernelizing
+ *    Tensor Programs" (gist.science/fr/paper/2512.22219), sections 2–4;
+ *  - the fused instructions (RMS norm, QKV matmul + RoPE, attention, O-proj
+ *    matmul + residual), matrix-vector tasks for low latency and
+ *    matrix-matrix tasks for throughput: "Llama-70B 向け…megakernel"
+ *    (hakusoku.com/story/2591), section 高スループットMegakernelの設計と工夫;
+ *  - residual + norm fusion and the fused SwiGLU feed-forward: "Cómo la
+ *    fusión de kernels CUDA acelera la inferencia de LLM" (slavadubrov.com),
+ *    section "Sigue los datos intermedios".
+ *
+ * Conventions for every function below:
+ *  - Memory: weights, KV pools, page table, tokens, positions and logits are
+ *    CALLER-OWNED device memory (unless a name ends in _host) and must stay
+ *    valid until the work queued on `stream` has finished.  The plan owns its
+ *    scratch, event counters, task tables, RoPE table and error word.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Calls are asynchronous on it unless stated otherwise.
+ *  - Errors that the host can detect return synchronously and launch nothing.
+ *    Errors found on the device (a wait that exceeded the plan's time budget,
+ *    an out-of-range token, position or page id) are recorded in the plan's
+ *    device error word; the kernel then exits without faulting.  Read them
+ *    with mk_plan_last_error.  The error stays set (and later steps return
+ *    early on the device) until mk_plan_last_error clears it.
+ *  - One plan is used by one stream at a time; calls that overlap on the GPU
+ *    race on the plan's scratch.
+ */
+#ifndef MK_H
+#define MK_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MK_OK = 0,
+    MK_ERR_INVALID = 1,     /* bad argument, null or misaligned pointer, bad shape */
+    MK_ERR_CUDA = 2,        /* a CUDA runtime call failed */
+    MK_ERR_LAUNCH = 3,      /* the cooperative grid cannot be co-resident */
+    MK_ERR_TIMEOUT = 4,     /* a device wait exceeded the plan's time budget */
+    MK_ERR_BOUNDS = 5,      /* token, position or page id out of range (device) */
+    MK_ERR_OOM = 6,         /* plan scratch allocation failed */
+    MK_ERR_UNSUPPORTED = 7  /* shape outside what this build implements */
+} mk_status;
+
+/* Decoder shape and the plan's fixed batch/context geometry. */
+typedef struct {
+    int32_t n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn_dim, vocab;
+    float rms_eps, rope_theta;
+    int32_t tied_embeddings; /* nonzero: lm_head == embed */
+    int32_t batch;           /* sequences per step, fixed per plan */
+    int32_t max_seq;         /* positions 0..max_seq-1 are valid */
+    int32_t page_size;       /* tokens per KV page */
+} mk_model_cfg;
+
+/* Weights: bf16, row-major [out][in], 16-byte aligned device pointers.
+ * Per-layer entries are HOST arrays of n_layers device pointers.
+ * Shapes: embed/lm_head [vocab][hidden]; final_norm, attn_norm, mlp_norm
+ * [hidden]; wq [n_q_heads*head_dim][hidden]; wk, wv [n_kv_heads*head_dim]
+ * [hidden]; wo [hidden][n_q_heads*head_dim]; w_gate, w_up [ffn_dim][hidden];
+ * w_down [hidden][ffn_dim].  Not modified and not copied: the plan keeps the
+ * pointers, so the weights must outlive the plan. */
+typedef struct {
+    const void *embed, *lm_head, *final_norm;
+    const void *const *attn_norm, *const *wq, *const *wk, *const *wv, *const *wo;
+    const void *const *mlp_norm, *const *w_gate, *const *w_up, *const *w_down;
+} mk_weight_ptrs;
+
+/* Paged KV cache (caller-owned).  Pools are bf16
+ * [n_layers][num_pages][n_kv_heads][page_size][head_dim]; page_table is a
+ * device int32 [batch][max_pages_per_seq]: token t of sequence b lives in
+ * page page_table[b][t / page_size], slot t % page_size. */
+typedef struct {
+    void *k_pool, *v_pool;
+    const int32_t *page_table;
+    int32_t num_pages, max_pages_per_seq;
+} mk_kv_cache;
+
+/* Optional plan knobs; zero fields take the defaults. */
+typedef struct {
+    int32_t num_ctas;      /* worker CTAs (default: every SM) */
+    int32_t attn_splits;   /* context splits per (sequence, kv head) (default: CTAs / (batch*n_kv_heads)) */
+    int32_t slot_bytes;    /* shared-memory ring slot size (default 32768) */
+    int32_t num_slots;     /* ring slots (default 6) */
+    int32_t timeout_ms;    /* budget of every device wait (default 2000) */
+    uint32_t planner_seed; /* nonzero: permute the CTA <-> tile assignment */
+    int32_t l2_prefetch_kb;/* per-CTA L2 prefetch distance ahead of the ring (default 0 = off) */
+    int32_t test_unreachable_event; /* failure-path testing: k > 0 makes the waiters of event k-1
+                                       need one signal more than can ever arrive, so their
+                                       bounded wait expires and the step reports MK_ERR_TIMEOUT */
+    int32_t reserved[8];
+} mk_plan_options;
+
+typedef struct mk_plan mk_plan; /* opaque, library-owned */
+
+/* Device error report. */
+typedef struct {
+    int32_t status; /* mk_status of the first device error, MK_OK if none */
+    int32_t site;   /* where it happened (see mk_error_site_string) */
+    int32_t cta;    /* worker CTA that recorded it */
+    int32_t detail; /* event id, task index or offending value */
+} mk_device_error;
+
+/* Build a plan for one decoder and batch geometry on the current device:
+ * validates the shape and pointer alignment, builds the task graph (per-CTA
+ * task queues and event thresholds), allocates the plan's scratch and
+ * checks that the cooperative grid fits.  Synchronous.  *out is set only on
+ * MK_OK.  MK_ERR_UNSUPPORTED: a shape this build does not implement. */
+mk_status mk_plan_create(const mk_model_cfg *cfg, const mk_weight_ptrs *w, mk_plan **out);
+mk_status mk_plan_create_ex(const mk_model_cfg *cfg, const mk_weight_ptrs *w, const mk_plan_options *opt,
+                            mk_plan **out);
+
+/* One decode step for every sequence of the batch: tokens[b] at position
+ * positions[b] (device int32 [batch]).  Appends K/V of that position to the
+ * cache, attends over positions 0..positions[b], writes logits (device fp32
+ * [batch][vocab]).  One cooperative launch. */
+mk_status mk_decode_step(mk_plan *plan, const int32_t *tokens, const int32_t *positions, const mk_kv_cache *kv,
+                         float *logits, void *stream);
+
+/* The same step, with the same task code, launched one kernel per operator
+ * and layer (5 per layer + 1), ordered by the stream instead of by event
+ * counters.  The launch-per-operator ablation of the megakernel. */
+mk_status mk_decode_step_ablation(mk_plan *plan, const int32_t *tokens, const int32_t *positions,
+                                  const mk_kv_cache *kv, float *logits, void *stream);
+
+/* mk_decode_step with HOST buffers: copies tokens/positions (host int32
+ * [batch]) in, runs the step, copies logits (host fp32 [batch][vocab]) out
+ * and synchronises `stream`.  Returns device errors of this step directly. */
+mk_status mk_decode_step_host(mk_plan *plan, const int32_t *tokens_host, const int32_t *positions_host,
+                              const mk_kv_cache *kv, float *logits_host, void *stream);
+
+/* Prefill T prompt tokens per sequence (device int32 [batch][T]) at
+ * positions 0..T-1 by running the decode step once per position; writes the
+ * logits of position T-1 (device fp32 [batch][vocab]).  The LM head runs only
+ * for the last position. */
+mk_status mk_prefill(mk_plan *plan, const int32_t *tokens, int32_t T, const mk_kv_cache *kv, float *last_logits,
+                     void *stream);
+
+/* Greedy continuation for the next step: tokens[b] = argmax_v logits[b][v]
+ * (lowest index on ties) and positions[b] += 1, on the device. */
+mk_status mk_greedy_next(mk_plan *plan, const float *logits, int32_t *tokens, int32_t *positions, void *stream);
+
+/* Synchronises `stream`, reads and clears the plan's device error word. */
+mk_status mk_plan_last_error(mk_plan *plan, void *stream, mk_device_error *info);
+
+const char *mk_status_string(mk_status s);
+const char *mk_error_site_string(int32_t site);
+
+/* Frees the plan's device memory.  Synchronises the device first. */
+void mk_plan_destroy(mk_plan *plan);
+
+/* ---------------------------------------------------------------------
+ * Host-only introspection of the task graph (no GPU needed).
+ * --------------------------------------------------------------------- */
+typedef struct {
+    int32_t cta;         /* worker CTA whose queue holds the task */
+    int32_t op;          /* 1 QKV, 2 ATTN, 3 O, 4 GATE_UP, 5 DOWN, 6 LM_HEAD */
+    int32_t layer;
+    int32_t wait_event;  /* -1: none */
+    int32_t wait_count;  /* proceed when counter[wait_event] >= wait_count */
+    int32_t signal_event;/* -1: none (attention: only the last split of a head signals) */
+    int32_t a0, a1;      /* matvec: output rows [a0, a1); attention: batch row, kv head */
+    int32_t a2, a3;      /* attention: split index, number of splits */
+} mk_task_info;
+
+/* Builds the task graph for `num_ctas` worker CTAs without touching a GPU.
+ * Writes up to `capacity` tasks (queue order, CTA by CTA) to out, the task
+ * count to *n_tasks and the number of event counters to *n_events.
+ * MK_ERR_INVALID if capacity is too small (n_tasks still set). */
+mk_status mk_plan_describe(const mk_model_cfg *cfg, const mk_plan_options *opt, int32_t num_ctas,
+                           mk_task_info *out, int32_t capacity, int32_t *n_tasks, int32_t *n_events);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MK_H */

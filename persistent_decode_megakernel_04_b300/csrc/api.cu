@@ -1,0 +1,412 @@
+// api.cu — C ABI of the decode megakernel (declared in include/mk.h).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/mk.h"
+#include "mk_kernel.h"
+#include "planner.h"
+
+using namespace mk;
+
+struct mk_plan {
+    mk_model_cfg cfg;
+    mk_plan_options opt;
+    PlanTables tables;
+    int device = 0;
+    int variant = 0;
+    size_t smem = 0;
+    CtlLayout cl{};
+    // device memory owned by the plan
+    std::vector<void *> allocs;
+    LayerW *d_layers = nullptr;
+    Task *d_tasks = nullptr;
+    int32_t *d_queue = nullptr;
+    float *d_x = nullptr, *d_qkv = nullptr, *d_part = nullptr, *d_attn = nullptr, *d_h = nullptr;
+    float2 *d_rope = nullptr;
+    uint32_t *d_ctl = nullptr;
+    int32_t *d_iota = nullptr;       // 0..max_seq-1, positions of prefill steps
+    int32_t *d_stage_tok = nullptr;  // staging for the host-buffer entry point
+    int32_t *d_stage_pos = nullptr;
+    float *d_stage_logits = nullptr;
+    KParams base{};
+};
+
+namespace {
+
+template <typename T>
+mk_status dev_alloc(mk_plan *p, T **ptr, size_t count) {
+    void *q = nullptr;
+    if (cudaMalloc(&q, std::max<size_t>(count, 1) * sizeof(T)) != cudaSuccess) {
+        cudaGetLastError();
+        return MK_ERR_OOM;
+    }
+    p->allocs.push_back(q);
+    *ptr = static_cast<T *>(q);
+    return MK_OK;
+}
+
+bool aligned16(const void *p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+mk_status check_weights(const mk_model_cfg &c, const mk_weight_ptrs *w) {
+    if (!w) return MK_ERR_INVALID;
+    if (!aligned16(w->embed) || !aligned16(w->lm_head) || !aligned16(w->final_norm)) return MK_ERR_INVALID;
+    if (c.tied_embeddings && w->lm_head != w->embed) return MK_ERR_INVALID;
+    const void *const *arrs[] = {w->attn_norm, w->wq, w->wk, w->wv, w->wo, w->mlp_norm, w->w_gate, w->w_up, w->w_down};
+    for (const void *const *a : arrs) {
+        if (!a) return MK_ERR_INVALID;
+        for (int l = 0; l < c.n_layers; ++l)
+            if (!aligned16(a[l])) return MK_ERR_INVALID;
+    }
+    return MK_OK;
+}
+
+mk_status check_kv(const mk_plan *p, const mk_kv_cache *kv) {
+    if (!kv || !aligned16(kv->k_pool) || !aligned16(kv->v_pool) || !aligned16(kv->page_table)) return MK_ERR_INVALID;
+    if (kv->num_pages <= 0 || kv->max_pages_per_seq <= 0) return MK_ERR_INVALID;
+    if ((int64_t)kv->max_pages_per_seq * p->cfg.page_size < p->cfg.max_seq) return MK_ERR_INVALID;
+    return MK_OK;
+}
+
+mk_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return MK_OK;
+    cudaGetLastError();
+    if (e == cudaErrorCooperativeLaunchTooLarge) return MK_ERR_LAUNCH;
+    return MK_ERR_CUDA;
+}
+
+void free_plan(mk_plan *p) {
+    for (void *q : p->allocs) cudaFree(q);
+    p->allocs.clear();
+    delete p;
+}
+
+KParams step_params(const mk_plan *p, const int32_t *tokens, int32_t tok_stride, const int32_t *positions,
+                    int32_t pos_stride, const mk_kv_cache *kv, float *logits) {
+    KParams k = p->base;
+    k.k_pool = static_cast<uint16_t *>(kv->k_pool);
+    k.v_pool = static_cast<uint16_t *>(kv->v_pool);
+    k.page_table = kv->page_table;
+    k.num_pages = kv->num_pages;
+    k.max_pages = kv->max_pages_per_seq;
+    k.tokens = tokens;
+    k.tok_stride = tok_stride;
+    k.positions = positions;
+    k.pos_stride = pos_stride;
+    k.logits = logits;
+    return k;
+}
+
+mk_status launch_step(mk_plan *p, const KParams &k, cudaStream_t s) {
+    cudaError_t e = cudaSetDevice(p->device);
+    if (e != cudaSuccess) return cuda_status(e);
+    return cuda_status(launch_megakernel(k, p->variant, p->tables.g.num_ctas, p->smem, true, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *mk_status_string(mk_status s) {
+    switch (s) {
+        case MK_OK: return "ok";
+        case MK_ERR_INVALID: return "invalid argument";
+        case MK_ERR_CUDA: return "CUDA runtime error";
+        case MK_ERR_LAUNCH: return "cooperative grid cannot be co-resident";
+        case MK_ERR_TIMEOUT: return "device wait exceeded the time budget";
+        case MK_ERR_BOUNDS: return "token, position or page id out of range";
+        case MK_ERR_OOM: return "out of device memory";
+        case MK_ERR_UNSUPPORTED: return "unsupported shape";
+    }
+    return "unknown status";
+}
+
+const char *mk_error_site_string(int32_t site) {
+    switch (site) {
+        case SITE_NONE: return "none";
+        case SITE_EVENT_WAIT: return "scheduler event-counter wait";
+        case SITE_READY_WAIT: return "compute wait for task release";
+        case SITE_FULL_WAIT: return "compute wait for a filled ring slot";
+        case SITE_EMPTY_WAIT: return "producer wait for a free ring slot";
+        case SITE_DRAIN_WAIT: return "producer drain of copies in flight";
+        case SITE_TOKEN: return "token id out of range";
+        case SITE_POSITION: return "position out of range";
+        case SITE_PAGE: return "page id out of range";
+        case SITE_ABORTED: return "aborted";
+    }
+    return "unknown site";
+}
+
+mk_status mk_plan_describe(const mk_model_cfg *cfg, const mk_plan_options *opt, int32_t num_ctas,
+                           mk_task_info *out, int32_t capacity, int32_t *n_tasks, int32_t *n_events) {
+    if (!cfg || num_ctas <= 0 || !n_tasks || !n_events) return MK_ERR_INVALID;
+    mk_plan_options o = resolve_options(*cfg, opt, num_ctas);
+    PlanTables t;
+    mk_status st = build_plan(*cfg, o, &t);
+    if (st != MK_OK) return st;
+    *n_tasks = (int32_t)t.tasks.size();
+    *n_events = t.g.n_events;
+    if (capacity < *n_tasks || (!out && *n_tasks > 0)) return MK_ERR_INVALID;
+    for (int32_t c = 0; c < o.num_ctas; ++c)
+        for (int32_t i = t.queue_off[c]; i < t.queue_off[c + 1]; ++i) {
+            const Task &k = t.tasks[i];
+            mk_task_info &d = out[i];
+            d.cta = c;
+            d.op = k.op;
+            d.layer = k.layer;
+            d.wait_event = k.wait_ev == kNoEvent ? -1 : k.wait_ev;
+            d.wait_count = (int32_t)k.wait_count;
+            d.signal_event = k.signal_ev == kNoEvent ? -1 : k.signal_ev;
+            d.a0 = k.a0;
+            d.a1 = k.a1;
+            d.a2 = k.a2;
+            d.a3 = k.a3;
+        }
+    return MK_OK;
+}
+
+mk_status mk_plan_create_ex(const mk_model_cfg *cfg, const mk_weight_ptrs *w, const mk_plan_options *opt,
+                            mk_plan **out) {
+    if (!cfg || !out) return MK_ERR_INVALID;
+    *out = nullptr;
+    mk_status st = check_cfg(*cfg);
+    if (st != MK_OK) return st;
+    if ((st = check_weights(*cfg, w)) != MK_OK) return st;
+
+    int dev = 0, sms = 0, smem_optin = 0, coop = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) ||
+        cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) ||
+        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev)) {
+        cudaGetLastError();
+        return MK_ERR_CUDA;
+    }
+    if (!coop) return MK_ERR_UNSUPPORTED;
+
+    mk_plan *p = new (std::nothrow) mk_plan();
+    if (!p) return MK_ERR_OOM;
+    p->cfg = *cfg;
+    p->device = dev;
+    p->opt = resolve_options(*cfg, opt, sms);
+    if (p->opt.num_slots > kMaxSlots) p->opt.num_slots = kMaxSlots;
+    if ((st = build_plan(*cfg, p->opt, &p->tables)) != MK_OK) {
+        free_plan(p);
+        return st;
+    }
+    PlanGeom &g = p->tables.g;
+    p->smem = megakernel_smem_bytes(g.slot_bytes, g.num_slots);
+    if ((int)p->smem > smem_optin) {
+        free_plan(p);
+        return MK_ERR_INVALID;
+    }
+    const int32_t max_k = std::max({cfg->hidden, cfg->ffn_dim, cfg->n_q_heads * cfg->head_dim});
+    p->variant = megakernel_variant(max_k);
+    if (megakernel_set_smem(p->variant, p->smem) != cudaSuccess) {
+        cudaGetLastError();
+        free_plan(p);
+        return MK_ERR_CUDA;
+    }
+    int per_sm = 0;
+    if (megakernel_max_active(p->variant, p->smem, &per_sm) != cudaSuccess || per_sm < 1) {
+        cudaGetLastError();
+        free_plan(p);
+        return MK_ERR_LAUNCH;
+    }
+
+    const mk_model_cfg &c = *cfg;
+    const int32_t G = c.n_q_heads / c.n_kv_heads, S = g.attn_splits;
+    const int32_t qkv_rows = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
+    p->cl = ctl_layout(g.n_events, c.batch * c.n_kv_heads);
+    const size_t n_part = (size_t)c.batch * c.n_kv_heads * S * G * (c.head_dim + 2);
+    if ((st = dev_alloc(p, &p->d_layers, c.n_layers)) || (st = dev_alloc(p, &p->d_tasks, p->tables.tasks.size())) ||
+        (st = dev_alloc(p, &p->d_queue, p->tables.queue_off.size())) ||
+        (st = dev_alloc(p, &p->d_x, (size_t)c.batch * c.hidden)) ||
+        (st = dev_alloc(p, &p->d_qkv, (size_t)c.batch * qkv_rows)) || (st = dev_alloc(p, &p->d_part, n_part)) ||
+        (st = dev_alloc(p, &p->d_attn, (size_t)c.batch * c.n_q_heads * c.head_dim)) ||
+        (st = dev_alloc(p, &p->d_h, (size_t)c.batch * c.ffn_dim)) ||
+        (st = dev_alloc(p, &p->d_rope, (size_t)c.max_seq * (c.head_dim / 2))) ||
+        (st = dev_alloc(p, &p->d_ctl, (size_t)p->cl.total)) || (st = dev_alloc(p, &p->d_iota, (size_t)c.max_seq)) ||
+        (st = dev_alloc(p, &p->d_stage_tok, (size_t)c.batch)) || (st = dev_alloc(p, &p->d_stage_pos, (size_t)c.batch)) ||
+        (st = dev_alloc(p, &p->d_stage_logits, (size_t)c.batch * c.vocab))) {
+        free_plan(p);
+        return st;
+    }
+
+    std::vector<LayerW> lw(c.n_layers);
+    for (int l = 0; l < c.n_layers; ++l) {
+        lw[l].attn_norm = static_cast<const uint16_t *>(w->attn_norm[l]);
+        lw[l].wq = static_cast<const uint16_t *>(w->wq[l]);
+        lw[l].wk = static_cast<const uint16_t *>(w->wk[l]);
+        lw[l].wv = static_cast<const uint16_t *>(w->wv[l]);
+        lw[l].wo = static_cast<const uint16_t *>(w->wo[l]);
+        lw[l].mlp_norm = static_cast<const uint16_t *>(w->mlp_norm[l]);
+        lw[l].w_gate = static_cast<const uint16_t *>(w->w_gate[l]);
+        lw[l].w_up = static_cast<const uint16_t *>(w->w_up[l]);
+        lw[l].w_down = static_cast<const uint16_t *>(w->w_down[l]);
+    }
+    std::vector<int32_t> iota(c.max_seq);
+    for (int32_t i = 0; i < c.max_seq; ++i) iota[i] = i;
+    cudaError_t e = cudaMemcpy(p->d_layers, lw.data(), lw.size() * sizeof(LayerW), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess)
+        e = cudaMemcpy(p->d_tasks, p->tables.tasks.data(), p->tables.tasks.size() * sizeof(Task),
+                       cudaMemcpyHostToDevice);
+    if (e == cudaSuccess)
+        e = cudaMemcpy(p->d_queue, p->tables.queue_off.data(), p->tables.queue_off.size() * sizeof(int32_t),
+                       cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(p->d_iota, iota.data(), iota.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemset(p->d_ctl, 0, (size_t)p->cl.total * sizeof(uint32_t));
+    if (e == cudaSuccess) e = launch_rope_table(p->d_rope, c.max_seq, c.head_dim, c.rope_theta, 0);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        free_plan(p);
+        return MK_ERR_CUDA;
+    }
+
+    KParams &k = p->base;
+    k.L = c.n_layers;
+    k.H = c.hidden;
+    k.nq = c.n_q_heads;
+    k.nkv = c.n_kv_heads;
+    k.d = c.head_dim;
+    k.I = c.ffn_dim;
+    k.V = c.vocab;
+    k.B = c.batch;
+    k.max_seq = c.max_seq;
+    k.page_size = c.page_size;
+    k.eps = c.rms_eps;
+    k.qkv_rows = qkv_rows;
+    k.embed = static_cast<const uint16_t *>(w->embed);
+    k.lm_head = static_cast<const uint16_t *>(w->lm_head);
+    k.final_norm = static_cast<const uint16_t *>(w->final_norm);
+    k.layers = p->d_layers;
+    k.x = p->d_x;
+    k.qkv = p->d_qkv;
+    k.attn_part = p->d_part;
+    k.attn_out = p->d_attn;
+    k.hbuf = p->d_h;
+    k.rope = p->d_rope;
+    k.ctl = p->d_ctl;
+    k.cl = p->cl;
+    k.tasks = p->d_tasks;
+    k.queue_off = p->d_queue;
+    for (int i = 0; i < OP_COUNT; ++i) k.mv[i] = g.mv[i];
+    k.slot_bytes = g.slot_bytes;
+    k.num_slots = g.num_slots;
+    k.tps = g.tps;
+    k.attn_splits = g.attn_splits;
+    k.l2_prefetch_bytes = g.l2_prefetch_bytes;
+    k.only_op = -1;
+    k.only_layer = -1;
+    k.skip_lm = 0;
+    k.timeout_ns = (uint64_t)p->opt.timeout_ms * 1000000ull;
+    *out = p;
+    return MK_OK;
+}
+
+mk_status mk_plan_create(const mk_model_cfg *cfg, const mk_weight_ptrs *w, mk_plan **out) {
+    return mk_plan_create_ex(cfg, w, nullptr, out);
+}
+
+mk_status mk_decode_step(mk_plan *p, const int32_t *tokens, const int32_t *positions, const mk_kv_cache *kv,
+                         float *logits, void *stream) {
+    if (!p || !tokens || !positions || !logits) return MK_ERR_INVALID;
+    mk_status st = check_kv(p, kv);
+    if (st != MK_OK) return st;
+    KParams k = step_params(p, tokens, 1, positions, 1, kv, logits);
+    return launch_step(p, k, static_cast<cudaStream_t>(stream));
+}
+
+mk_status mk_decode_step_ablation(mk_plan *p, const int32_t *tokens, const int32_t *positions,
+                                  const mk_kv_cache *kv, float *logits, void *stream) {
+    if (!p || !tokens || !positions || !logits) return MK_ERR_INVALID;
+    mk_status st = check_kv(p, kv);
+    if (st != MK_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaSetDevice(p->device) != cudaSuccess) return cuda_status(cudaGetLastError());
+    KParams k = step_params(p, tokens, 1, positions, 1, kv, logits);
+    static const int kOps[] = {OP_QKV, OP_ATTN, OP_O, OP_GU, OP_DOWN};
+    for (int l = 0; l < p->cfg.n_layers; ++l)
+        for (int op : kOps) {
+            k.only_op = op;
+            k.only_layer = l;
+            st = cuda_status(launch_megakernel(k, p->variant, p->tables.g.num_ctas, p->smem, false, s));
+            if (st != MK_OK) return st;
+        }
+    k.only_op = OP_LM;
+    k.only_layer = p->cfg.n_layers - 1;
+    return cuda_status(launch_megakernel(k, p->variant, p->tables.g.num_ctas, p->smem, false, s));
+}
+
+mk_status mk_prefill(mk_plan *p, const int32_t *tokens, int32_t T, const mk_kv_cache *kv, float *last_logits,
+                     void *stream) {
+    if (!p || !tokens || !last_logits || T <= 0 || T > p->cfg.max_seq) return MK_ERR_INVALID;
+    mk_status st = check_kv(p, kv);
+    if (st != MK_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    for (int32_t t = 0; t < T; ++t) {
+        KParams k = step_params(p, tokens + t, T, p->d_iota + t, 0, kv, last_logits);
+        k.skip_lm = (t + 1 < T) ? 1 : 0;
+        if ((st = launch_step(p, k, s)) != MK_OK) return st;
+    }
+    return MK_OK;
+}
+
+mk_status mk_greedy_next(mk_plan *p, const float *logits, int32_t *tokens, int32_t *positions, void *stream) {
+    if (!p || !logits || !tokens || !positions) return MK_ERR_INVALID;
+    return cuda_status(launch_greedy_next(logits, p->cfg.batch, p->cfg.vocab, tokens, positions,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+mk_status mk_plan_last_error(mk_plan *p, void *stream, mk_device_error *info) {
+    if (!p) return MK_ERR_INVALID;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t words[4] = {0, 0, 0, 0};
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess)
+        e = cudaMemcpy(words, p->d_ctl + p->cl.err_idx, sizeof(words), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (words[0] != 0) {
+        // clear the error, the abort flag and every counter for the next launch
+        e = cudaMemset(p->d_ctl, 0, (size_t)p->cl.total * sizeof(uint32_t));
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    if (info) {
+        info->status = (int32_t)words[0];
+        info->site = (int32_t)words[1];
+        info->cta = (int32_t)words[2];
+        info->detail = (int32_t)words[3];
+    }
+    return (mk_status)words[0];
+}
+
+mk_status mk_decode_step_host(mk_plan *p, const int32_t *tokens_host, const int32_t *positions_host,
+                              const mk_kv_cache *kv, float *logits_host, void *stream) {
+    if (!p || !tokens_host || !positions_host || !logits_host) return MK_ERR_INVALID;
+    mk_status st = check_kv(p, kv);
+    if (st != MK_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t nb = (size_t)p->cfg.batch * sizeof(int32_t);
+    cudaError_t e = cudaMemcpyAsync(p->d_stage_tok, tokens_host, nb, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(p->d_stage_pos, positions_host, nb, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_status(e);
+    KParams k = step_params(p, p->d_stage_tok, 1, p->d_stage_pos, 1, kv, p->d_stage_logits);
+    if ((st = launch_step(p, k, s)) != MK_OK) return st;
+    e = cudaMemcpyAsync(logits_host, p->d_stage_logits, (size_t)p->cfg.batch * p->cfg.vocab * sizeof(float),
+                        cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_status(e);
+    return mk_plan_last_error(p, stream, nullptr);
+}
+
+void mk_plan_destroy(mk_plan *p) {
+    if (!p) return;
+    cudaSetDevice(p->device);
+    cudaDeviceSynchronize();
+    free_plan(p);
+}
+
+}  // extern "C"

@@ -1,0 +1,195 @@
+// planner.cpp — host task-graph builder.
+//
+// Refines the decoder's operator graph into SM-level tasks linked by event
+// counters, in the manner of the task graph the MPK compiler emits ("Compilar
+// LLM en un MegaKernel…", section "Parte 1. Compilador": each task is a unit
+// of work for one SM, events are synchronisation points between tasks, and
+// dependencies are tracked at the level of the data actually consumed) and
+// of the SM-level tGraph ("MPK: A Compiler and Runtime for Mega-Kernelizing
+// Tensor Programs", section 2).
+//
+// Per layer, in queue order:
+//   QKV  : RMSNorm + [Wq;Wk;Wv] rows          waits x ready      signals EV(QKV)
+//   ATTN : RoPE + KV append + split attention waits EV(QKV)       last split signals EV(ATTN)
+//   O    : split merge + Wo rows + residual    waits EV(ATTN)     signals EV(O)
+//   GU   : RMSNorm + gate/up rows + SiLU*mul   waits EV(O)        signals EV(GU)
+//   DOWN : Wd rows + residual                  waits EV(GU)       signals EV(DOWN)
+// then the LM head (final RMSNorm + W_lm rows) waits the last EV(DOWN).
+// Every matvec operator's rows are cut into one contiguous range per worker
+// CTA, balanced to within one row; the schedule is fixed ahead of time for a
+// (shape, batch) pair, because only the attention length changes between
+// steps, and that is resolved on the device from the positions.
+#include "planner.h"
+
+#include <algorithm>
+#include <cstring>
+#include <numeric>
+#include <random>
+
+namespace mk {
+
+namespace {
+
+int32_t round_up(int32_t a, int32_t b) { return (a + b - 1) / b * b; }
+
+MvGeom make_geom(int32_t K, int32_t rows, int32_t row_mult, int32_t slot_bytes) {
+    MvGeom g{};
+    g.K = K;
+    g.rows = rows;
+    g.row_mult = row_mult;
+    const int32_t piece_max = slot_bytes / row_mult;
+    const int32_t max_rows = 8 / row_mult;  // accumulators per thread stay <= 8
+    if (K * 2 <= piece_max) {
+        g.ksplit = 1;
+        g.kc = K;
+        g.rpp = std::min(max_rows, piece_max / (K * 2));
+    } else {
+        g.ksplit = (K * 2 + piece_max - 1) / piece_max;
+        for (;;) {
+            g.kc = round_up((K + g.ksplit - 1) / g.ksplit, 8);
+            if (g.kc * 2 <= piece_max) break;
+            ++g.ksplit;
+        }
+        g.rpp = 1;
+    }
+    return g;
+}
+
+}  // namespace
+
+mk_status check_cfg(const mk_model_cfg &c) {
+    if (c.n_layers <= 0 || c.hidden <= 0 || c.n_q_heads <= 0 || c.n_kv_heads <= 0 || c.head_dim <= 0 ||
+        c.ffn_dim <= 0 || c.vocab <= 0 || c.batch <= 0 || c.max_seq <= 0 || c.page_size <= 0)
+        return MK_ERR_INVALID;
+    if (c.n_q_heads % c.n_kv_heads != 0) return MK_ERR_INVALID;
+    if (!(c.rms_eps >= 0.0f) || !(c.rope_theta > 0.0f)) return MK_ERR_INVALID;
+    // 16-byte copies need every row length to be a multiple of 8 bf16
+    if (c.hidden % 8 || c.ffn_dim % 8 || c.head_dim % 64) return MK_ERR_UNSUPPORTED;
+    if (c.n_layers * 5 >= 0xFFFF) return MK_ERR_UNSUPPORTED;
+    const int32_t group = c.n_q_heads / c.n_kv_heads;
+    if (group > 8 || c.head_dim > 128) return MK_ERR_UNSUPPORTED;
+    if (c.batch != 1) return MK_ERR_UNSUPPORTED;  // batched (tensor-core) tiles: not in this build yet
+    return MK_OK;
+}
+
+mk_plan_options resolve_options(const mk_model_cfg &cfg, const mk_plan_options *opt, int32_t num_sms) {
+    mk_plan_options o;
+    std::memset(&o, 0, sizeof(o));
+    if (opt) o = *opt;
+    if (o.num_ctas <= 0 || o.num_ctas > num_sms) o.num_ctas = num_sms;
+    if (o.slot_bytes <= 0) o.slot_bytes = 32768;
+    if (o.num_slots <= 0) o.num_slots = 6;
+    if (o.timeout_ms <= 0) o.timeout_ms = 2000;
+    if (o.attn_splits <= 0) {
+        int32_t pairs = cfg.batch * cfg.n_kv_heads;
+        o.attn_splits = std::max(1, o.num_ctas / std::max(1, pairs));
+    }
+    if (o.l2_prefetch_kb < 0) o.l2_prefetch_kb = 0;
+    return o;
+}
+
+mk_status build_plan(const mk_model_cfg &cfg, const mk_plan_options &opt, PlanTables *out) {
+    mk_status st = check_cfg(cfg);
+    if (st != MK_OK) return st;
+    const int32_t N = opt.num_ctas;
+    if (N <= 0 || opt.slot_bytes < 4096 || opt.slot_bytes % 1024 || opt.num_slots < 2 || opt.attn_splits <= 0)
+        return MK_ERR_INVALID;
+    const int32_t H = cfg.hidden, d = cfg.head_dim, nq = cfg.n_q_heads, nkv = cfg.n_kv_heads;
+    const int32_t I = cfg.ffn_dim, V = cfg.vocab, L = cfg.n_layers, B = cfg.batch, S = opt.attn_splits;
+
+    PlanGeom &g = out->g;
+    g = PlanGeom{};
+    g.num_ctas = N;
+    g.attn_splits = S;
+    g.slot_bytes = opt.slot_bytes;
+    g.num_slots = opt.num_slots;
+    g.tps = std::min(128, opt.slot_bytes / (2 * d * 2));
+    g.n_events = 5 * L;
+    g.l2_prefetch_bytes = opt.l2_prefetch_kb * 1024;
+    g.mv[OP_QKV] = make_geom(H, (nq + 2 * nkv) * d, 1, opt.slot_bytes);
+    g.mv[OP_O] = make_geom(nq * d, H, 1, opt.slot_bytes);
+    g.mv[OP_GU] = make_geom(H, I, 2, opt.slot_bytes);
+    g.mv[OP_DOWN] = make_geom(I, H, 1, opt.slot_bytes);
+    g.mv[OP_LM] = make_geom(H, V, 1, opt.slot_bytes);
+    if (g.tps < 1) return MK_ERR_INVALID;
+
+    // CTA permutation (identity unless a planner seed is given)
+    std::vector<int32_t> perm(N);
+    std::iota(perm.begin(), perm.end(), 0);
+    if (opt.planner_seed) {
+        std::mt19937 rng(opt.planner_seed);
+        std::shuffle(perm.begin(), perm.end(), rng);
+    }
+
+    std::vector<std::vector<Task>> q(N);
+    auto emit_matvec = [&](int32_t op, int32_t layer, int32_t rows, uint16_t wait_ev, uint32_t wait_cnt,
+                           uint16_t sig_ev) -> uint32_t {
+        uint32_t n = 0;
+        for (int32_t c = 0; c < N; ++c) {
+            int32_t r0 = (int32_t)((int64_t)c * rows / N), r1 = (int32_t)((int64_t)(c + 1) * rows / N);
+            if (r1 <= r0) continue;
+            Task t{};
+            t.op = (uint8_t)op;
+            t.layer = (uint16_t)layer;
+            t.wait_ev = wait_ev;
+            t.wait_count = wait_cnt;
+            t.signal_ev = sig_ev;
+            t.a0 = r0;
+            t.a1 = r1;
+            q[perm[c]].push_back(t);
+            ++n;
+        }
+        return n;
+    };
+    auto count_ranges = [&](int32_t rows) { return (uint32_t)std::min<int64_t>(rows, N); };
+
+    const uint32_t n_qkv = count_ranges(g.mv[OP_QKV].rows), n_o = count_ranges(H), n_gu = count_ranges(I),
+                   n_down = count_ranges(H);
+    uint16_t x_ready_ev = kNoEvent;
+    uint32_t x_ready_cnt = 0;
+    for (int32_t l = 0; l < L; ++l) {
+        uint32_t k = emit_matvec(OP_QKV, l, g.mv[OP_QKV].rows, x_ready_ev, x_ready_cnt, (uint16_t)ev_id(l, OP_QKV));
+        if (k != n_qkv) return MK_ERR_INVALID;
+        // attention: one task per (sequence, kv head, split), round-robin over CTAs
+        int32_t i = 0;
+        for (int32_t b = 0; b < B; ++b)
+            for (int32_t h = 0; h < nkv; ++h)
+                for (int32_t s = 0; s < S; ++s, ++i) {
+                    Task t{};
+                    t.op = OP_ATTN;
+                    t.layer = (uint16_t)l;
+                    t.wait_ev = (uint16_t)ev_id(l, OP_QKV);
+                    t.wait_count = n_qkv;
+                    t.signal_ev = (uint16_t)ev_id(l, OP_ATTN);
+                    t.a0 = b;
+                    t.a1 = h;
+                    t.a2 = s;
+                    t.a3 = S;
+                    q[perm[i % N]].push_back(t);
+                }
+        emit_matvec(OP_O, l, H, (uint16_t)ev_id(l, OP_ATTN), (uint32_t)(B * nkv), (uint16_t)ev_id(l, OP_O));
+        emit_matvec(OP_GU, l, I, (uint16_t)ev_id(l, OP_O), n_o, (uint16_t)ev_id(l, OP_GU));
+        emit_matvec(OP_DOWN, l, H, (uint16_t)ev_id(l, OP_GU), n_gu, (uint16_t)ev_id(l, OP_DOWN));
+        x_ready_ev = (uint16_t)ev_id(l, OP_DOWN);
+        x_ready_cnt = n_down;
+    }
+    emit_matvec(OP_LM, L - 1, V, x_ready_ev, x_ready_cnt, kNoEvent);
+
+    if (opt.test_unreachable_event > 0) {
+        const int32_t ev = opt.test_unreachable_event - 1;
+        if (ev >= g.n_events) return MK_ERR_INVALID;
+        for (auto &qq : q)
+            for (Task &t : qq)
+                if (t.wait_ev == ev) ++t.wait_count;
+    }
+    out->tasks.clear();
+    out->queue_off.assign(N + 1, 0);
+    for (int32_t c = 0; c < N; ++c) {
+        out->queue_off[c] = (int32_t)out->tasks.size();
+        out->tasks.insert(out->tasks.end(), q[c].begin(), q[c].end());
+    }
+    out->queue_off[N] = (int32_t)out->tasks.size();
+    return MK_OK;
+}
+
+}  // namespace mk

@@ -1,0 +1,43 @@
+// planner.h — host task-graph builder of the decode megakernel.
+#pragma once
+
+#include <vector>
+
+#include "../../include/mk.h"
+#include "mk_types.h"
+
+namespace mk {
+
+struct PlanGeom {
+    int32_t num_ctas = 0;
+    int32_t attn_splits = 0;
+    int32_t slot_bytes = 0;
+    int32_t num_slots = 0;
+    int32_t tps = 0;  // KV tokens per ring slot
+    int32_t n_events = 0;
+    int32_t l2_prefetch_bytes = 0;
+    MvGeom mv[OP_COUNT] = {};
+};
+
+struct PlanTables {
+    PlanGeom g;
+    std::vector<Task> tasks;          // CTA 0's queue, then CTA 1's, ...
+    std::vector<int32_t> queue_off;   // [num_ctas + 1]
+};
+
+// Fills in defaults for zero option fields.
+mk_plan_options resolve_options(const mk_model_cfg &cfg, const mk_plan_options *opt, int32_t num_sms);
+
+// Shape checks shared by plan creation and the host-only describe call.
+mk_status check_cfg(const mk_model_cfg &cfg);
+
+// Builds the task graph for cfg on opt.num_ctas worker CTAs.
+mk_status build_plan(const mk_model_cfg &cfg, const mk_plan_options &opt, PlanTables *out);
+
+// Event ids.
+inline int32_t ev_id(int32_t layer, int32_t op) {
+    // per layer: QKV, ATTN, O, GU, DOWN
+    return layer * 5 + (op - 1);
+}
+
+}  // namespace mk

@@ -1,0 +1,217 @@
+"""GPU parity: the megakernel (through the C ABI) against the fp64 oracle on
+the same seeded inputs.  Tolerances are the parity contract's: final logits
+rel-L2 <= 1e-2 and max-abs <= 3e-2, greedy token equal whenever the oracle's
+top-2 gap exceeds 0.05 (tests/harness.py)."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import persistent_decode_megakernel_04_b300 as mk
+import synth
+from synth import WORKLOADS
+from tests import harness
+
+pytestmark = pytest.mark.gpu
+
+TINY = WORKLOADS["tiny"].model
+
+
+def _bits(t):
+    import torch
+
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def test_device_generator_matches_host_bit_for_bit(cuda_device):
+    import torch
+
+    for shape, tid, sig, off in [((4099,), 5, 0.02, 0.0), ((1000, 37), 17, 0.5, 0.0), ((513,), 3, 0.1, 1.0)]:
+        t = torch.empty(shape, dtype=torch.bfloat16, device=cuda_device)
+        synth._fill_device(t, 7, tid, sig, off)
+        assert np.array_equal(_bits(t), synth.normal_bf16(shape, 7, tid, sig, off))
+    # every tensor of the tiny model, and sampled rows of the 8B-shaped embedding
+    dw, hw = synth.device_weights(TINY, 0), synth.host_weights(TINY, 0)
+    assert np.array_equal(_bits(dw["embed"]), hw["embed"])
+    for l in range(TINY.n_layers):
+        for k in hw["layers"][l]:
+            assert np.array_equal(_bits(dw["layers"][l][k]), hw["layers"][l][k]), (l, k)
+    big = WORKLOADS["8b"].model
+    t = torch.empty((64, big.hidden), dtype=torch.bfloat16, device=cuda_device)
+    synth._fill_device(t, 0, synth.TID_EMBED, big.weight_std)
+    assert np.array_equal(_bits(t), synth.normal_bf16((64, big.hidden), 0, synth.TID_EMBED, big.weight_std))
+
+
+def test_device_kv_page_fill_matches_host(cuda_device):
+    m = TINY
+    kv = mk.KVCache(m, 2, 200, shuffle_seed=3)
+    synth.device_kv_pages(kv.k[1], kv.page_table, m, 0, 1, "k", 2, kv.max_pages, 150, kv.page_size)
+    ref = synth.host_kv(m, 0, 1, "k", 2, 150)
+    pt = kv.page_table.cpu().numpy()
+    pool = _bits(kv.k[1])
+    for b in range(2):
+        for t in (0, 63, 64, 149):
+            assert np.array_equal(pool[pt[b, t // 64], :, t % 64, :], ref[b, t])
+
+
+@pytest.mark.parametrize("gains", [False, True], ids=["unit-gains", "random-gains"])
+def test_tiny_prompt_and_greedy_decode(cuda_device, gains):
+    m = synth.with_random_gains(TINY) if gains else TINY
+    wl = WORKLOADS["tiny"]
+    max_seq = wl.seq_capacity
+    plan, kv = harness.gpu_plan(m, max_seq)
+    model = harness.oracle_model(m)
+    prompt = synth.tokens(wl.prompt_len, 0, 0, m.vocab)
+    stats = harness.run_teacher_forced(plan, kv, model, prompt, wl.decode_steps, max_seq)
+    assert len(stats) == wl.decode_steps + 1
+
+
+def test_tiny_ablation_matches_oracle(cuda_device):
+    wl = WORKLOADS["tiny"]
+    plan, kv = harness.gpu_plan(TINY, wl.seq_capacity)
+    model = harness.oracle_model(TINY)
+    prompt = synth.tokens(wl.prompt_len, 0, 1, TINY.vocab)
+    harness.run_teacher_forced(plan, kv, model, prompt, 8, wl.seq_capacity, ablation_every=1)
+
+
+def test_tiny_reduced_grid_and_permuted_schedule(cuda_device):
+    # fewer worker CTAs than rows, odd split counts and a shuffled CTA assignment
+    for opts in (mk.mk_plan_options(num_ctas=7, attn_splits=3, planner_seed=5),
+                 mk.mk_plan_options(num_ctas=148, attn_splits=1, num_slots=2, slot_bytes=8192, planner_seed=9)):
+        plan, kv = harness.gpu_plan(TINY, 128, opts=opts)
+        model = harness.oracle_model(TINY)
+        prompt = synth.tokens(70, 0, 2, TINY.vocab)  # crosses a KV page boundary
+        harness.run_teacher_forced(plan, kv, model, prompt, 4, 128)
+
+
+def test_host_buffer_entry_point_and_greedy_next(cuda_device):
+    import torch
+
+    wl = WORKLOADS["tiny"]
+    plan, kv = harness.gpu_plan(TINY, wl.seq_capacity)
+    prompt = synth.tokens(9, 0, 3, TINY.vocab)
+    toks = torch.tensor(prompt, dtype=torch.int32, device=cuda_device).view(1, -1)
+    logits = torch.empty((1, TINY.vocab), dtype=torch.float32, device=cuda_device)
+    plan.prefill(toks, kv, logits)
+    nxt = torch.empty(1, dtype=torch.int32, device=cuda_device)
+    pos = torch.full((1,), 8, dtype=torch.int32, device=cuda_device)
+    plan.greedy_next(logits, nxt, pos)
+    ref_tok = int(np.argmax(logits.cpu().numpy()[0]))
+    assert int(nxt.item()) == ref_tok and int(pos.item()) == 9
+    # the host-buffer call equals the device call at the same position
+    host_logits = np.empty((1, TINY.vocab), dtype=np.float32)
+    plan.decode_step_host(np.array([ref_tok], np.int32), np.array([9], np.int32), kv, host_logits)
+    dev_logits = torch.empty_like(logits)
+    plan.decode_step(nxt, pos, kv, dev_logits)
+    plan.check()
+    assert np.array_equal(host_logits, dev_logits.cpu().numpy())
+
+
+def test_repeated_steps_are_bitwise_deterministic(cuda_device):
+    import torch
+
+    wl = WORKLOADS["tiny"]
+    plan, kv = harness.gpu_plan(TINY, wl.seq_capacity)
+    toks = torch.tensor(synth.tokens(20, 0, 4, TINY.vocab), dtype=torch.int32, device=cuda_device).view(1, -1)
+    logits = torch.empty((1, TINY.vocab), dtype=torch.float32, device=cuda_device)
+    plan.prefill(toks, kv, logits)
+    t = torch.tensor([5], dtype=torch.int32, device=cuda_device)
+    p = torch.tensor([20], dtype=torch.int32, device=cuda_device)
+    outs = []
+    for _ in range(3):
+        plan.decode_step(t, p, kv, logits)  # rewrites the same cache slot
+        outs.append(logits.cpu().numpy().copy())
+    plan.check()
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
+
+
+def test_out_of_range_token_and_position_are_reported_not_faulted(cuda_device):
+    import torch
+
+    wl = WORKLOADS["tiny"]
+    plan, kv = harness.gpu_plan(TINY, wl.seq_capacity)
+    logits = torch.empty((1, TINY.vocab), dtype=torch.float32, device=cuda_device)
+    good_t = torch.tensor([3], dtype=torch.int32, device=cuda_device)
+    good_p = torch.tensor([0], dtype=torch.int32, device=cuda_device)
+    for tok, pos, site in ((TINY.vocab, 0, 6), (-1, 0, 6), (3, wl.seq_capacity, 7), (3, -5, 7)):
+        t = torch.tensor([tok], dtype=torch.int32, device=cuda_device)
+        p = torch.tensor([pos], dtype=torch.int32, device=cuda_device)
+        plan.decode_step(t, p, kv, logits)
+        info = plan.last_error()
+        assert info.status == mk.MK_ERR_BOUNDS and info.site == site
+        # the error was cleared by reading it: a valid step runs again
+        plan.decode_step(good_t, good_p, kv, logits)
+        assert plan.last_error().status == mk.MK_OK
+    assert np.all(np.isfinite(logits.cpu().numpy()))
+
+
+def test_bad_page_id_is_reported_not_faulted(cuda_device):
+    import torch
+
+    plan, kv = harness.gpu_plan(TINY, 128)
+    logits = torch.empty((1, TINY.vocab), dtype=torch.float32, device=cuda_device)
+    kv.page_table[0, 1] = kv.num_pages  # one past the pool
+    plan.decode_step(torch.tensor([3], dtype=torch.int32, device=cuda_device),
+                     torch.tensor([70], dtype=torch.int32, device=cuda_device), kv, logits)
+    info = plan.last_error()
+    assert info.status == mk.MK_ERR_BOUNDS and info.site == 8 and info.detail == kv.num_pages
+
+
+def test_unreachable_event_times_out_cleanly(cuda_device):
+    import torch
+
+    wl = WORKLOADS["tiny"]
+    # waiters of layer 0's attention event need one more signal than exists
+    opts = mk.mk_plan_options(timeout_ms=100, test_unreachable_event=2)
+    plan, kv = harness.gpu_plan(TINY, wl.seq_capacity, opts=opts)
+    logits = torch.empty((1, TINY.vocab), dtype=torch.float32, device=cuda_device)
+    t = torch.tensor([3], dtype=torch.int32, device=cuda_device)
+    p = torch.tensor([0], dtype=torch.int32, device=cuda_device)
+    plan.decode_step(t, p, kv, logits)
+    info = plan.last_error()
+    assert info.status == mk.MK_ERR_TIMEOUT and info.site == 1 and info.detail == 1
+    # the context is intact: a normal plan on the same device still matches the oracle
+    good, kv2 = harness.gpu_plan(TINY, wl.seq_capacity)
+    model = harness.oracle_model(TINY)
+    harness.run_teacher_forced(good, kv2, model, synth.tokens(5, 0, 5, TINY.vocab), 2, wl.seq_capacity)
+
+
+def test_invalid_kv_descriptor_rejected_on_host(cuda_device):
+    import torch
+
+    plan, kv = harness.gpu_plan(TINY, 128)
+    logits = torch.empty((1, TINY.vocab), dtype=torch.float32, device=cuda_device)
+    t = torch.tensor([3], dtype=torch.int32, device=cuda_device)
+    d = kv.desc
+    bads = [mk.mk_kv_cache(d.k_pool, d.v_pool, d.page_table, d.num_pages, 1),  # 64 positions < max_seq 128
+            mk.mk_kv_cache(d.k_pool + 2, d.v_pool, d.page_table, d.num_pages, d.max_pages_per_seq),  # misaligned
+            mk.mk_kv_cache(d.k_pool, None, d.page_table, d.num_pages, d.max_pages_per_seq),
+            mk.mk_kv_cache(d.k_pool, d.v_pool, d.page_table, 0, d.max_pages_per_seq)]
+    for bad in bads:
+        st = mk.lib().mk_decode_step(plan.h, t.data_ptr(), t.data_ptr(), ctypes.byref(bad), logits.data_ptr(),
+                                     None)
+        assert st == mk.MK_ERR_INVALID
+    assert mk.lib().mk_decode_step(plan.h, t.data_ptr(), t.data_ptr(), ctypes.byref(d), None, None) == \
+        mk.MK_ERR_INVALID
+
+
+def test_tiny_long_prompt_through_decode_path(cuda_device):
+    # 130-token prompt: several KV pages, splits that straddle pages
+    plan, kv = harness.gpu_plan(TINY, 256)
+    model = harness.oracle_model(TINY)
+    harness.run_teacher_forced(plan, kv, model, synth.tokens(130, 0, 6, TINY.vocab), 3, 256)
+
+
+@pytest.mark.parametrize("name,ctx,steps", [("1b", 512, 3), ("8b", 39, 3), ("8b-batch", 4096, 2)])
+def test_full_size_decode_from_seeded_cache(cuda_device, name, ctx, steps):
+    """Full-size shapes in the launch configuration the bench times (every
+    SM, default ring): decode steps at the workload's context length, from a
+    seeded stand-in cache that both sides read."""
+    wl = WORKLOADS[name]
+    m = wl.model
+    max_seq = ((ctx + steps + 64) // 64) * 64
+    plan, kv = harness.gpu_plan(m, max_seq)
+    model = harness.oracle_model(m)
+    caches = harness.fill_synthetic_cache(kv, model, m, ctx, 1, max_seq)
+    stats = harness.run_from_cache(plan, kv, model, caches, ctx, steps, synth.tokens(1, wl.seed, 0, m.vocab))
+    print(name, stats)

@@ -1,0 +1,137 @@
+"""Host task-graph builder: coverage, event thresholds and a simulated run of
+the per-CTA queues (the device runtime's semantics, executed on the CPU)."""
+from collections import defaultdict
+
+import pytest
+
+import persistent_decode_megakernel_04_b300 as mk
+from synth import WORKLOADS
+
+SHAPES = {
+    "tiny": WORKLOADS["tiny"].model,
+    "1b": WORKLOADS["1b"].model,
+    "8b": WORKLOADS["8b"].model,
+}
+
+
+def describe(name, num_ctas, **kw):
+    m = SHAPES[name]
+    cfg = mk.model_cfg(m, 1, 1024)
+    opts = mk.mk_plan_options(**kw) if kw else None
+    tasks, n_events = mk.mk_plan_describe(cfg, num_ctas, opts)
+    return m, tasks, n_events
+
+
+def op_rows(m, op):
+    d = m.head_dim
+    return {mk.OP_QKV: (m.n_q_heads + 2 * m.n_kv_heads) * d, mk.OP_O: m.hidden, mk.OP_GU: m.ffn_dim,
+            mk.OP_DOWN: m.hidden, mk.OP_LM: m.vocab}[op]
+
+
+@pytest.mark.parametrize("name", list(SHAPES))
+@pytest.mark.parametrize("num_ctas", [148, 37, 1])
+def test_every_output_row_covered_exactly_once(name, num_ctas):
+    m, tasks, _ = describe(name, num_ctas)
+    cover = defaultdict(list)
+    for t in tasks:
+        if t.op != mk.OP_ATTN:
+            cover[(t.layer, t.op)].append((t.a0, t.a1))
+    for l in range(m.n_layers):
+        for op in (mk.OP_QKV, mk.OP_O, mk.OP_GU, mk.OP_DOWN):
+            rs = sorted(cover[(l, op)])
+            assert rs[0][0] == 0 and rs[-1][1] == op_rows(m, op)
+            assert all(a[1] == b[0] for a, b in zip(rs, rs[1:])), "gap or overlap"
+            sizes = [b - a for a, b in rs]
+            assert max(sizes) - min(sizes) <= 1, "row ranges balanced to one row"
+    lm = sorted(cover[(m.n_layers - 1, mk.OP_LM)])
+    assert lm[0][0] == 0 and lm[-1][1] == m.vocab
+
+
+@pytest.mark.parametrize("name", list(SHAPES))
+def test_attention_tasks_cover_every_head_and_split(name):
+    m, tasks, _ = describe(name, 148)
+    att = [t for t in tasks if t.op == mk.OP_ATTN]
+    S = att[0].a3
+    assert S == max(1, 148 // m.n_kv_heads)
+    seen = {(t.layer, t.a0, t.a1, t.a2) for t in att}
+    assert len(seen) == len(att) == m.n_layers * m.n_kv_heads * S
+
+
+def test_queue_order_is_stage_order_within_each_cta():
+    _, tasks, _ = describe("8b", 148)
+    stage = lambda t: (t.layer, t.op)
+    by_cta = defaultdict(list)
+    for t in tasks:
+        by_cta[t.cta].append(stage(t))
+    for q in by_cta.values():
+        assert q == sorted(q)
+
+
+def simulate(m, tasks, n_events):
+    """Runs the queues with event counters as the device does: a CTA's next task
+    may run once counter[wait] >= wait_count; attention signals once per
+    (sequence, kv head), when its last split finishes."""
+    queues = defaultdict(list)
+    for t in tasks:
+        queues[t.cta].append(t)
+    head = {c: 0 for c in queues}
+    ctr = [0] * n_events
+    done_splits = defaultdict(int)
+    order = []
+    progress = True
+    while progress:
+        progress = False
+        for c, q in queues.items():
+            while head[c] < len(q):
+                t = q[head[c]]
+                if t.wait_event >= 0 and ctr[t.wait_event] < t.wait_count:
+                    break
+                if t.op == mk.OP_ATTN:
+                    k = (t.layer, t.a0, t.a1)
+                    done_splits[k] += 1
+                    if done_splits[k] == t.a3:
+                        ctr[t.signal_event] += 1
+                elif t.signal_event >= 0:
+                    ctr[t.signal_event] += 1
+                order.append(t)
+                head[c] += 1
+                progress = True
+    return all(head[c] == len(q) for c, q in queues.items()), order, ctr
+
+
+@pytest.mark.parametrize("name", list(SHAPES))
+@pytest.mark.parametrize("num_ctas,seed", [(148, 0), (148, 7), (5, 3)])
+def test_schedule_completes_and_respects_dependencies(name, num_ctas, seed):
+    m, tasks, n_events = describe(name, num_ctas, planner_seed=seed)
+    ok, order, ctr = simulate(m, tasks, n_events)
+    assert ok, "deadlock: some queue never drained"
+    expect = {}
+    for t in tasks:
+        if t.wait_event >= 0:
+            assert expect.setdefault(t.wait_event, t.wait_count) == t.wait_count
+    for e, cnt in expect.items():
+        assert ctr[e] == cnt
+    pos = {}
+    for i, t in enumerate(order):
+        pos.setdefault((t.layer, t.op), []).append(i)
+    for l in range(m.n_layers):
+        assert min(pos[(l, mk.OP_ATTN)]) > max(pos[(l, mk.OP_QKV)])
+        assert min(pos[(l, mk.OP_O)]) > max(pos[(l, mk.OP_ATTN)])
+        assert min(pos[(l, mk.OP_GU)]) > max(pos[(l, mk.OP_O)])
+        assert min(pos[(l, mk.OP_DOWN)]) > max(pos[(l, mk.OP_GU)])
+        if l + 1 < m.n_layers:
+            assert min(pos[(l + 1, mk.OP_QKV)]) > max(pos[(l, mk.OP_DOWN)])
+
+
+def test_unreachable_event_option_blocks_the_schedule():
+    m, tasks, n_events = describe("tiny", 148, test_unreachable_event=2)
+    ok, _, _ = simulate(m, tasks, n_events)
+    assert not ok
+
+
+def test_planner_seed_permutes_assignment_but_not_work():
+    _, a, _ = describe("tiny", 148)
+    _, b, _ = describe("tiny", 148, planner_seed=11)
+    key = lambda t: (t.layer, t.op, t.a0, t.a1, t.a2)
+    assert sorted(map(key, a)) == sorted(map(key, b))
+    assert [t.cta for t in sorted(a, key=key)] != [t.cta for t in sorted(b, key=key)]
