@@ -40,12 +40,19 @@ METRIC = "decode ms/token (batch 1) + achieved HBM GB/s vs B300 peak per step"
 FALLBACK_HBM_GBS = 6400.0
 
 
+def weight_bytes_read(m, batch: int) -> int:
+    """bf16 weight bytes one decode step must read: every layer matrix and
+    gain, the final gain and the LM head once, one embedding row per sequence."""
+    per_layer = sum(int(np.prod(s)) for s in synth.layer_shapes(m).values())
+    return 2 * (m.n_layers * per_layer + m.vocab * m.hidden + m.hidden + batch * m.hidden)
+
+
 def step_bytes(m, batch: int, ctx: int) -> int:
     """Algorithmic HBM bytes of one decode step at context length ctx (the new
-    token included): every weight once, every cached K/V entry once, the new
+    token included): the weights above, every cached K/V entry once, the new
     K/V entry written once, the logits written once."""
     per_tok = 2 * m.n_layers * m.n_kv_heads * m.head_dim * 2  # K and V, all layers, bf16
-    return synth.weight_bytes(m) + batch * (per_tok * (ctx - 1) + per_tok + m.vocab * 4)
+    return weight_bytes_read(m, batch) + batch * (per_tok * (ctx - 1) + per_tok + m.vocab * 4)
 
 
 def measured_peak():
@@ -264,6 +271,23 @@ def run_mk(args, wl):
         abl["ctx"] = int(pos_a[0].item()) + 1
         plan.check()
 
+    if args.trace_out and rank == 0:
+        # one more step with a tracing plan over the same weights and cache
+        from persistent_decode_megakernel_04_b300 import trace as mktrace
+
+        topt = mk.mk_plan_options(trace=1)
+        tplan = mk.Plan(m, weights, batch=B, max_seq=max_seq, opts=topt)
+        tpos = h_pos.to(dev)
+        for _ in range(2):
+            tplan.decode_step(h_tok.to(dev), tpos, kv, logits)
+        tr = tplan.trace()
+        tplan.check()
+        tasks, _ = mk.mk_plan_describe(tplan.cfg, tr.shape[0], topt)
+        rows = mktrace.phases(tasks, tr)
+        Path(args.trace_out).write_text(json.dumps(rows, indent=1))
+        Path(args.trace_out).with_suffix(".chrome.json").write_text(mktrace.chrome_trace(tasks, tr))
+        tplan.close()
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         ms, threads, desc = oracle_sample(m, args.cpu_samples, wl.prompt_len)
@@ -309,9 +333,13 @@ def main():
     ap.add_argument("--ablation-steps", type=int, default=8)
     ap.add_argument("--cpu-samples", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prompt-len", type=int, default=0, help="override the workload's prompt length")
+    ap.add_argument("--trace-out", default="", help="write a per-phase task trace of one extra step here")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     wl = WORKLOADS[args.workload]
+    if args.prompt_len > 0:
+        wl = replace(wl, prompt_len=args.prompt_len)
     if args.impl == "reference":
         run_reference(args, wl)
     else:

@@ -107,7 +107,8 @@ typedef struct {
     int32_t test_unreachable_event; /* failure-path testing: k > 0 makes the waiters of event k-1
                                        need one signal more than can ever arrive, so their
                                        bounded wait expires and the step reports MK_ERR_TIMEOUT */
-    int32_t reserved[8];
+    int32_t trace;         /* nonzero: record per-task timestamps (see mk_plan_trace) */
+    int32_t reserved[7];
 } mk_plan_options;
 
 typedef struct mk_plan mk_plan; /* opaque, library-owned */
@@ -158,6 +159,20 @@ mk_status mk_prefill(mk_plan *plan, const int32_t *tokens, int32_t T, const mk_k
 /* Greedy continuation for the next step: tokens[b] = argmax_v logits[b][v]
  * (lowest index on ties) and positions[b] += 1, on the device. */
 mk_status mk_greedy_next(mk_plan *plan, const float *logits, int32_t *tokens, int32_t *positions, void *stream);
+
+/* Task trace of the last step run with a plan created with options.trace:
+ * for every CTA c and queue position i (the order of mk_plan_describe),
+ * out[(c * *max_tasks + i) * 8 + k] holds, in globaltimer nanoseconds,
+ *   k=0 scheduler released the task (its event reached the threshold),
+ *   k=1 compute warps started it, k=2 they finished it,
+ *   k=3 total time the compute warps waited for ring slots to fill,
+ *   k=4 producer issued the task's first copy,
+ *   k=5 total time the producer waited for free ring slots.
+ * Zeros mark tasks not run.  Synchronises `stream`.  Host buffer of
+ * `capacity` uint64 values; MK_ERR_INVALID if tracing is off or the buffer is
+ * too small (*max_tasks is still set). */
+mk_status mk_plan_trace(mk_plan *plan, void *stream, uint64_t *out, int64_t capacity, int32_t *num_ctas,
+                        int32_t *max_tasks);
 
 /* Synchronises `stream`, reads and clears the plan's device error word. */
 mk_status mk_plan_last_error(mk_plan *plan, void *stream, mk_device_error *info);

@@ -41,7 +41,7 @@ class mk_kv_cache(ctypes.Structure):
 class mk_plan_options(ctypes.Structure):
     _fields_ = [("num_ctas", _i32), ("attn_splits", _i32), ("slot_bytes", _i32), ("num_slots", _i32),
                 ("timeout_ms", _i32), ("planner_seed", ctypes.c_uint32), ("l2_prefetch_kb", _i32),
-                ("test_unreachable_event", _i32), ("reserved", _i32 * 8)]
+                ("test_unreachable_event", _i32), ("trace", _i32), ("reserved", _i32 * 7)]
 
 
 class mk_device_error(ctypes.Structure):
@@ -56,7 +56,7 @@ class mk_task_info(ctypes.Structure):
 _lib = None
 EXPORTS = ("mk_plan_create", "mk_plan_create_ex", "mk_decode_step", "mk_decode_step_ablation",
            "mk_decode_step_host", "mk_prefill", "mk_greedy_next", "mk_plan_last_error", "mk_status_string",
-           "mk_error_site_string", "mk_plan_destroy", "mk_plan_describe")
+           "mk_error_site_string", "mk_plan_destroy", "mk_plan_describe", "mk_plan_trace")
 
 
 def lib():
@@ -83,6 +83,7 @@ def lib():
         L.mk_plan_destroy.restype = None
         L.mk_plan_describe.argtypes = [P(mk_model_cfg), P(mk_plan_options), _i32, P(mk_task_info), _i32,
                                        P(_i32), P(_i32)]
+        L.mk_plan_trace.argtypes = [_vp, _vp, _vp, ctypes.c_int64, P(_i32), P(_i32)]
         for n in EXPORTS:
             if n not in ("mk_plan_destroy", "mk_status_string", "mk_error_site_string"):
                 getattr(L, n).restype = ctypes.c_int
@@ -222,6 +223,17 @@ class Plan:
         info = mk_device_error()
         lib().mk_plan_last_error(self.h, _stream_ptr(stream), ctypes.byref(info))
         return info
+
+    def trace(self, stream=None):
+        """numpy uint64 [num_ctas][max_tasks][8] of the last step (plan built with trace=1)."""
+        import numpy as np
+
+        nc, mt = _i32(0), _i32(0)
+        lib().mk_plan_trace(self.h, _stream_ptr(stream), None, 0, ctypes.byref(nc), ctypes.byref(mt))
+        out = np.zeros((nc.value, mt.value, 8), dtype=np.uint64)
+        _check(lib().mk_plan_trace(self.h, _stream_ptr(stream), out.ctypes.data, out.size, ctypes.byref(nc),
+                                   ctypes.byref(mt)), "mk_plan_trace")
+        return out
 
     def check(self, stream=None) -> None:
         info = self.last_error(stream)

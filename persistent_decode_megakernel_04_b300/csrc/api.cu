@@ -33,6 +33,8 @@ struct mk_plan {
     int32_t *d_stage_tok = nullptr;  // staging for the host-buffer entry point
     int32_t *d_stage_pos = nullptr;
     float *d_stage_logits = nullptr;
+    uint64_t *d_trace = nullptr;
+    int32_t trace_stride = 0;
     KParams base{};
 };
 
@@ -101,9 +103,17 @@ KParams step_params(const mk_plan *p, const int32_t *tokens, int32_t tok_stride,
     return k;
 }
 
+mk_status clear_trace(mk_plan *p, cudaStream_t s) {
+    if (!p->d_trace) return MK_OK;
+    return cuda_status(
+        cudaMemsetAsync(p->d_trace, 0, (size_t)p->tables.g.num_ctas * p->trace_stride * 8 * sizeof(uint64_t), s));
+}
+
 mk_status launch_step(mk_plan *p, const KParams &k, cudaStream_t s) {
     cudaError_t e = cudaSetDevice(p->device);
     if (e != cudaSuccess) return cuda_status(e);
+    mk_status st = clear_trace(p, s);
+    if (st != MK_OK) return st;
     return cuda_status(launch_megakernel(k, p->variant, p->tables.g.num_ctas, p->smem, true, s));
 }
 
@@ -234,6 +244,14 @@ mk_status mk_plan_create_ex(const mk_model_cfg *cfg, const mk_weight_ptrs *w, co
         free_plan(p);
         return st;
     }
+    if (p->opt.trace) {
+        for (int32_t i = 0; i < g.num_ctas; ++i)
+            p->trace_stride = std::max(p->trace_stride, p->tables.queue_off[i + 1] - p->tables.queue_off[i]);
+        if ((st = dev_alloc(p, &p->d_trace, (size_t)g.num_ctas * p->trace_stride * 8)) != MK_OK) {
+            free_plan(p);
+            return st;
+        }
+    }
 
     std::vector<LayerW> lw(c.n_layers);
     for (int l = 0; l < c.n_layers; ++l) {
@@ -303,6 +321,8 @@ mk_status mk_plan_create_ex(const mk_model_cfg *cfg, const mk_weight_ptrs *w, co
     k.only_layer = -1;
     k.skip_lm = 0;
     k.timeout_ns = (uint64_t)p->opt.timeout_ms * 1000000ull;
+    k.trace = p->d_trace;
+    k.trace_stride = p->trace_stride;
     *out = p;
     return MK_OK;
 }
@@ -328,6 +348,7 @@ mk_status mk_decode_step_ablation(mk_plan *p, const int32_t *tokens, const int32
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaSetDevice(p->device) != cudaSuccess) return cuda_status(cudaGetLastError());
     KParams k = step_params(p, tokens, 1, positions, 1, kv, logits);
+    if ((st = clear_trace(p, s)) != MK_OK) return st;
     static const int kOps[] = {OP_QKV, OP_ATTN, OP_O, OP_GU, OP_DOWN};
     for (int l = 0; l < p->cfg.n_layers; ++l)
         for (int op : kOps) {
@@ -400,6 +421,18 @@ mk_status mk_decode_step_host(mk_plan *p, const int32_t *tokens_host, const int3
                         cudaMemcpyDeviceToHost, s);
     if (e != cudaSuccess) return cuda_status(e);
     return mk_plan_last_error(p, stream, nullptr);
+}
+
+mk_status mk_plan_trace(mk_plan *p, void *stream, uint64_t *out, int64_t capacity, int32_t *num_ctas,
+                        int32_t *max_tasks) {
+    if (!p || !p->d_trace) return MK_ERR_INVALID;
+    if (num_ctas) *num_ctas = p->tables.g.num_ctas;
+    if (max_tasks) *max_tasks = p->trace_stride;
+    const int64_t n = (int64_t)p->tables.g.num_ctas * p->trace_stride * 8;
+    if (!out || capacity < n) return MK_ERR_INVALID;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) e = cudaMemcpy(out, p->d_trace, (size_t)n * sizeof(uint64_t), cudaMemcpyDeviceToHost);
+    return cuda_status(e);
 }
 
 void mk_plan_destroy(mk_plan *p) {

@@ -77,6 +77,10 @@ __device__ __forceinline__ bool task_active(const KParams &p, const Task &t) {
     return true;
 }
 
+__device__ __forceinline__ uint64_t *trace_slot(const KParams &p, int task) {
+    return p.trace ? p.trace + ((size_t)blockIdx.x * p.trace_stride + task) * 8 : nullptr;
+}
+
 __device__ __forceinline__ bool global_abort(const KParams &p) {
     return ld_relaxed_gpu(p.ctl + p.cl.abort_idx) != 0;
 }
@@ -183,11 +187,18 @@ __device__ __forceinline__ int64_t kv_offset(const KParams &p, int layer, int32_
 struct Producer {
     uint32_t issued = 0;
     uint64_t pol;
+    uint64_t *tr = nullptr;  // trace entry of the current task
 
     __device__ bool acquire_slot(const Ctx &c, uint32_t *slot) {
         const uint32_t s = issued % (uint32_t)c.p->num_slots;
         const uint32_t round = issued / (uint32_t)c.p->num_slots;
+        const uint64_t t0 = tr ? globaltimer_ns() : 0;
         if (!wait_mbar(c, &c.sc->empty[s], (round & 1u) ^ 1u, SITE_EMPTY_WAIT)) return false;
+        if (tr) {
+            const uint64_t t1 = globaltimer_ns();
+            if (tr[4] == 0) tr[4] = t1;
+            tr[5] += t1 - t0;
+        }
         *slot = s;
         return true;
     }
@@ -277,6 +288,7 @@ __device__ void producer_role(const Ctx &c, const Task *q, int nt) {
     for (int i = 0; i < nt; ++i) {
         const Task t = q[i];
         if (!task_active(*c.p, t)) continue;
+        pr.tr = trace_slot(*c.p, i);
         const bool ok = (t.op == OP_ATTN) ? pr.run_attn(c, t) : pr.run_matvec(c, t);
         if (!ok) break;
     }
@@ -312,6 +324,7 @@ __device__ void scheduler_role(const Ctx &c, const Task *q, int nt) {
                 }
             }
         }
+        if (uint64_t *tr = trace_slot(p, i)) tr[0] = globaltimer_ns();
         st_release_cta(&c.sc->ready, (uint32_t)(i + 1));
     }
 }
@@ -348,6 +361,8 @@ struct Consumer {
     uint32_t consumed = 0;
     int ct, wc, lane;  // compute-thread index, compute-warp index, lane
     uint32_t red_buf = 0;
+    bool tracing = false;
+    uint64_t full_wait_ns = 0;
 
     // A failed wait (abort or timeout) marks the CTA aborted but keeps the
     // control flow: all compute warps must reach the same named barriers, so
@@ -355,7 +370,9 @@ struct Consumer {
     __device__ uint32_t wait_slot(const Ctx &c) {
         const uint32_t s = consumed % (uint32_t)c.p->num_slots;
         const uint32_t round = consumed / (uint32_t)c.p->num_slots;
+        const uint64_t t0 = tracing ? globaltimer_ns() : 0;
         wait_mbar(c, &c.sc->full[s], round & 1u, SITE_FULL_WAIT);
+        if (tracing) full_wait_ns += globaltimer_ns() - t0;
         return s;
     }
 
@@ -708,6 +725,7 @@ __device__ void compute_role(const Ctx &c, const Task *q, int nt) {
     cs.ct = threadIdx.x - 64;
     cs.wc = cs.ct >> 5;
     cs.lane = threadIdx.x & 31;
+    cs.tracing = p.trace != nullptr && cs.ct == 0;
     for (int i = 0; i < nt; ++i) {
         const Task t = q[i];
         if (!task_active(p, t)) continue;
@@ -727,9 +745,16 @@ __device__ void compute_role(const Ctx &c, const Task *q, int nt) {
         }
         compute_bar();  // every compute warp sees the same abort state
         if (local_abort(c)) return;
+        uint64_t *tr = cs.tracing ? trace_slot(p, i) : nullptr;
+        if (tr) tr[1] = globaltimer_ns();
         if (t.op == OP_ATTN) cs.run_attn(c, t);
         else cs.run_matvec<MAXCH>(c, t);
         compute_bar();  // every output row of the task is written
+        if (tr) {
+            tr[2] = globaltimer_ns();
+            tr[3] = cs.full_wait_ns;
+            cs.full_wait_ns = 0;
+        }
         if (local_abort(c)) return;
         if (t.op != OP_ATTN && p.only_op < 0 && t.signal_ev != kNoEvent && cs.ct == 0) {
             __threadfence();

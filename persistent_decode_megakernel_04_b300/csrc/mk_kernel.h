@@ -52,6 +52,9 @@ struct KParams {
     int32_t only_layer;
     int32_t skip_lm;     // prefill positions before the last: no LM head
     uint64_t timeout_ns;
+    // optional task trace: [num_ctas][trace_stride][8] globaltimer stamps
+    uint64_t *trace;
+    int32_t trace_stride;
 };
 
 // Shared memory the megakernel needs for a given ring.
