@@ -167,6 +167,12 @@ def run_reference(args, wl):
 
 # ----------------------------------------------------------------- GPU side
 
+def seeded_context(wl) -> bool:
+    """Contexts of 1024 tokens and more are seeded into the paged cache
+    instead of prefilled token by token."""
+    return wl.prompt_len >= 1024
+
+
 def run_mk(args, wl):
     import torch
     import torch.distributed as dist
@@ -186,14 +192,24 @@ def run_mk(args, wl):
     weights = synth.device_weights(m, wl.seed, device=dev)
     plan = mk.Plan(m, weights, batch=B, max_seq=max_seq)
     kv = mk.KVCache(m, B, max_seq, shuffle_seed=1, device=dev)
-    prompt = np.stack([synth.tokens(wl.prompt_len, wl.seed, b, m.vocab) for b in range(B)])
-    toks = torch.tensor(prompt, dtype=torch.int32, device=dev)
     logits = torch.empty((B, m.vocab), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    plan.prefill(toks, kv, logits)
     tok = torch.empty(B, dtype=torch.int32, device=dev)
     pos = torch.full((B,), wl.prompt_len - 1, dtype=torch.int32, device=dev)
-    plan.greedy_next(logits, tok, pos)  # first generated token, at position prompt_len
+    if seeded_context(wl):
+        # long contexts: the paged cache of positions [0, prompt_len) is filled
+        # with seeded values (as if prefilled), then decode starts there
+        for l in range(m.n_layers):
+            synth.device_kv_pages(kv.k[l], kv.page_table, m, wl.seed, l, "k", B, kv.max_pages, wl.prompt_len,
+                                  kv.page_size)
+            synth.device_kv_pages(kv.v[l], kv.page_table, m, wl.seed, l, "v", B, kv.max_pages, wl.prompt_len,
+                                  kv.page_size)
+        tok.copy_(torch.tensor(synth.tokens(B, wl.seed, 0, m.vocab), dtype=torch.int32))
+        pos.fill_(wl.prompt_len)
+    else:
+        prompt = np.stack([synth.tokens(wl.prompt_len, wl.seed, b, m.vocab) for b in range(B)])
+        plan.prefill(torch.tensor(prompt, dtype=torch.int32, device=dev), kv, logits)
+        plan.greedy_next(logits, tok, pos)  # first generated token, at position prompt_len
     for _ in range(args.warmup):
         plan.decode_step(tok, pos, kv, logits)
         plan.greedy_next(logits, tok, pos)
@@ -300,6 +316,7 @@ def run_mk(args, wl):
             "vs_baseline": None, "dtype": "bf16 weights/KV, fp32 math",
             "data": "synthetic (seeded random-init weights, random prompt ids)",
             "config": {"workload": args.workload, "model": m.name, "batch": B, "prompt_len": wl.prompt_len,
+                       "context": "seeded paged cache" if seeded_context(wl) else "prefilled prompt",
                        "ctx_first_timed": ctx0, "ctx_last_timed": ctx0 + args.steps - 1,
                        "parallelism": f"replicas x{world}",
                        "l2": "no flush: ~15 GB of weights stream per step (> 126 MB L2)"},
@@ -334,12 +351,15 @@ def main():
     ap.add_argument("--cpu-samples", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prompt-len", type=int, default=0, help="override the workload's prompt length")
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (sequences per step)")
     ap.add_argument("--trace-out", default="", help="write a per-phase task trace of one extra step here")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     wl = WORKLOADS[args.workload]
     if args.prompt_len > 0:
         wl = replace(wl, prompt_len=args.prompt_len)
+    if args.batch > 0:
+        wl = replace(wl, batch=args.batch)
     if args.impl == "reference":
         run_reference(args, wl)
     else:

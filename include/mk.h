@@ -67,7 +67,8 @@ typedef struct {
     int32_t n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn_dim, vocab;
     float rms_eps, rope_theta;
     int32_t tied_embeddings; /* nonzero: lm_head == embed */
-    int32_t batch;           /* sequences per step, fixed per plan */
+    int32_t batch;           /* sequences per step, fixed per plan (1: CUDA-core matvec path;
+                                2..64: tensor-core path) */
     int32_t max_seq;         /* positions 0..max_seq-1 are valid */
     int32_t page_size;       /* tokens per KV page */
 } mk_model_cfg;
@@ -98,7 +99,8 @@ typedef struct {
 /* Optional plan knobs; zero fields take the defaults. */
 typedef struct {
     int32_t num_ctas;      /* worker CTAs (default: every SM) */
-    int32_t attn_splits;   /* context splits per (sequence, kv head) (default: CTAs / (batch*n_kv_heads)) */
+    int32_t attn_splits;   /* context splits per (sequence, kv head), at most 64
+                              (default: CTAs / (batch*n_kv_heads), capped at 64) */
     int32_t slot_bytes;    /* shared-memory ring slot size (default 32768) */
     int32_t num_slots;     /* ring slots (default 6) */
     int32_t timeout_ms;    /* budget of every device wait (default 2000) */
@@ -188,13 +190,16 @@ void mk_plan_destroy(mk_plan *plan);
  * --------------------------------------------------------------------- */
 typedef struct {
     int32_t cta;         /* worker CTA whose queue holds the task */
-    int32_t op;          /* 1 QKV, 2 ATTN, 3 O, 4 GATE_UP, 5 DOWN, 6 LM_HEAD */
+    int32_t op;          /* 1 QKV, 2 ATTN, 3 O, 4 GATE_UP, 5 DOWN, 6 LM_HEAD, 7 EMBED (batched only) */
     int32_t layer;
     int32_t wait_event;  /* -1: none */
     int32_t wait_count;  /* proceed when counter[wait_event] >= wait_count */
     int32_t signal_event;/* -1: none (attention: only the last split of a head signals) */
-    int32_t a0, a1;      /* matvec: output rows [a0, a1); attention: batch row, kv head */
-    int32_t a2, a3;      /* attention: split index, number of splits */
+    int32_t a0, a1;      /* batch 1 projection: output rows [a0, a1);
+                            batched projection: units [a0, a1), unit u = 128-row tile u / ceil(K/64),
+                            64-column chunk u % ceil(K/64); embedding: items [a0, a1), item =
+                            sequence * ceil(hidden/128) + 128-row tile; attention: batch row, kv head */
+    int32_t a2, a3;      /* attention: split index, number of splits; projections: range number a2 */
 } mk_task_info;
 
 /* Builds the task graph for `num_ctas` worker CTAs without touching a GPU.

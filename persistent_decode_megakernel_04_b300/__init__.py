@@ -13,7 +13,8 @@ import ctypes
 from .build import LIB, build
 
 MK_OK, MK_ERR_INVALID, MK_ERR_CUDA, MK_ERR_LAUNCH, MK_ERR_TIMEOUT, MK_ERR_BOUNDS, MK_ERR_OOM, MK_ERR_UNSUPPORTED = range(8)
-OP_QKV, OP_ATTN, OP_O, OP_GU, OP_DOWN, OP_LM = range(1, 7)
+OP_QKV, OP_ATTN, OP_O, OP_GU, OP_DOWN, OP_LM, OP_EMBED = range(1, 8)
+TC_TILE_M, TC_TILE_K = 128, 64  # batched path: weight rows x columns per unit
 
 _i32, _f32, _vp = ctypes.c_int32, ctypes.c_float, ctypes.c_void_p
 

@@ -1,4 +1,6 @@
 // api.cu — C ABI of the decode megakernel (declared in include/mk.h).
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -10,6 +12,7 @@
 #include "../../include/mk.h"
 #include "mk_kernel.h"
 #include "planner.h"
+#include "ptx.cuh"
 
 using namespace mk;
 
@@ -35,6 +38,10 @@ struct mk_plan {
     float *d_stage_logits = nullptr;
     uint64_t *d_trace = nullptr;
     int32_t trace_stride = 0;
+    // batched path
+    uint16_t *d_xa = nullptr, *d_attn_a = nullptr, *d_h_a = nullptr;
+    float *d_ssq = nullptr, *d_tc_part = nullptr;
+    uint8_t *d_tmaps = nullptr;
     KParams base{};
 };
 
@@ -72,6 +79,37 @@ mk_status check_kv(const mk_plan *p, const mk_kv_cache *kv) {
     if (kv->num_pages <= 0 || kv->max_pages_per_seq <= 0) return MK_ERR_INVALID;
     if ((int64_t)kv->max_pages_per_seq * p->cfg.page_size < p->cfg.max_seq) return MK_ERR_INVALID;
     return MK_OK;
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once (no libcuda link).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        else
+            cudaGetLastError();
+    }
+    return fn;
+}
+
+// Row-major bf16 [outer][inner] matrix read in boxes of 64 columns x
+// box_outer rows, 128-byte swizzled (the tcgen05 K-major operand layout).
+// Rows and columns past the end read as zero.
+bool encode_bf16_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {inner * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kTcTileK, box_outer};
+    const cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 mk_status cuda_status(cudaError_t e) {
@@ -207,13 +245,23 @@ mk_status mk_plan_create_ex(const mk_model_cfg *cfg, const mk_weight_ptrs *w, co
         return st;
     }
     PlanGeom &g = p->tables.g;
-    p->smem = megakernel_smem_bytes(g.slot_bytes, g.num_slots);
+    if (g.tc && g.num_slots == 0) {
+        // as many weight tiles in flight as shared memory holds
+        const size_t fixed = megakernel_smem_bytes(0, 0, g.aslot_bytes, g.num_aslots);
+        g.num_slots = (int32_t)std::min<size_t>(kMaxSlots, ((size_t)smem_optin - fixed) / g.slot_bytes);
+        p->opt.num_slots = g.num_slots;
+        if (g.num_slots < 2) {
+            free_plan(p);
+            return MK_ERR_UNSUPPORTED;
+        }
+    }
+    p->smem = megakernel_smem_bytes(g.slot_bytes, g.num_slots, g.tc ? g.aslot_bytes : 0, g.tc ? g.num_aslots : 0);
     if ((int)p->smem > smem_optin) {
         free_plan(p);
         return MK_ERR_INVALID;
     }
     const int32_t max_k = std::max({cfg->hidden, cfg->ffn_dim, cfg->n_q_heads * cfg->head_dim});
-    p->variant = megakernel_variant(max_k);
+    p->variant = megakernel_variant(max_k, g.tc);
     if (megakernel_set_smem(p->variant, p->smem) != cudaSuccess) {
         cudaGetLastError();
         free_plan(p);
@@ -229,7 +277,7 @@ mk_status mk_plan_create_ex(const mk_model_cfg *cfg, const mk_weight_ptrs *w, co
     const mk_model_cfg &c = *cfg;
     const int32_t G = c.n_q_heads / c.n_kv_heads, S = g.attn_splits;
     const int32_t qkv_rows = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
-    p->cl = ctl_layout(g.n_events, c.batch * c.n_kv_heads);
+    p->cl = ctl_layout(g.n_events, c.batch * c.n_kv_heads, g.tc ? g.n_tile_ctrs : 0);
     const size_t n_part = (size_t)c.batch * c.n_kv_heads * S * G * (c.head_dim + 2);
     if ((st = dev_alloc(p, &p->d_layers, c.n_layers)) || (st = dev_alloc(p, &p->d_tasks, p->tables.tasks.size())) ||
         (st = dev_alloc(p, &p->d_queue, p->tables.queue_off.size())) ||
@@ -243,6 +291,19 @@ mk_status mk_plan_create_ex(const mk_model_cfg *cfg, const mk_weight_ptrs *w, co
         (st = dev_alloc(p, &p->d_stage_logits, (size_t)c.batch * c.vocab))) {
         free_plan(p);
         return st;
+    }
+    const int32_t n_tmaps = c.n_layers * 7 + 4;
+    if (g.tc) {
+        const size_t part = (size_t)g.num_ctas * 2 * 2 * g.npad * kTcTileM;
+        const size_t rows2 = 2 * (size_t)g.npad;  // split-bf16 operands: high parts, then low parts
+        if ((st = dev_alloc(p, &p->d_xa, rows2 * c.hidden)) ||
+            (st = dev_alloc(p, &p->d_attn_a, rows2 * c.n_q_heads * c.head_dim)) ||
+            (st = dev_alloc(p, &p->d_h_a, rows2 * c.ffn_dim)) ||
+            (st = dev_alloc(p, &p->d_ssq, (size_t)c.batch * g.h_tiles)) || (st = dev_alloc(p, &p->d_tc_part, part)) ||
+            (st = dev_alloc(p, &p->d_tmaps, (size_t)n_tmaps * sizeof(CUtensorMap)))) {
+            free_plan(p);
+            return st;
+        }
     }
     if (p->opt.trace) {
         for (int32_t i = 0; i < g.num_ctas; ++i)
@@ -275,6 +336,34 @@ mk_status mk_plan_create_ex(const mk_model_cfg *cfg, const mk_weight_ptrs *w, co
         e = cudaMemcpy(p->d_queue, p->tables.queue_off.data(), p->tables.queue_off.size() * sizeof(int32_t),
                        cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemcpy(p->d_iota, iota.data(), iota.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess && g.tc) {
+        // tensor maps of every weight matrix (128-row boxes) and of the three
+        // activation operands (npad-row boxes; rows past the batch read as 0)
+        const int32_t H = c.hidden, I = c.ffn_dim, qd = c.n_q_heads * c.head_dim, kd = c.n_kv_heads * c.head_dim;
+        std::vector<CUtensorMap> maps(n_tmaps);
+        bool ok = true;
+        for (int l = 0; l < c.n_layers && ok; ++l) {
+            CUtensorMap *m = &maps[(size_t)l * 7];
+            ok = encode_bf16_2d(m + 0, w->wq[l], H, qd, kTcTileM) && encode_bf16_2d(m + 1, w->wk[l], H, kd, kTcTileM) &&
+                 encode_bf16_2d(m + 2, w->wv[l], H, kd, kTcTileM) && encode_bf16_2d(m + 3, w->wo[l], qd, H, kTcTileM) &&
+                 encode_bf16_2d(m + 4, w->w_gate[l], H, I, kTcTileM) &&
+                 encode_bf16_2d(m + 5, w->w_up[l], H, I, kTcTileM) && encode_bf16_2d(m + 6, w->w_down[l], I, H, kTcTileM);
+        }
+        CUtensorMap *m = &maps[(size_t)c.n_layers * 7];
+        ok = ok && encode_bf16_2d(m + 0, w->lm_head, H, c.vocab, kTcTileM) &&
+             encode_bf16_2d(m + 1, p->d_xa, H, 2 * g.npad, 2 * g.npad) &&
+             encode_bf16_2d(m + 2, p->d_attn_a, qd, 2 * g.npad, 2 * g.npad) &&
+             encode_bf16_2d(m + 3, p->d_h_a, I, 2 * g.npad, 2 * g.npad);
+        if (!ok) {
+            free_plan(p);
+            return MK_ERR_CUDA;
+        }
+        e = cudaMemcpy(p->d_tmaps, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice);
+        // padding rows (sequences past the batch) stay zero
+        if (e == cudaSuccess) e = cudaMemset(p->d_xa, 0, 2 * (size_t)g.npad * c.hidden * 2);
+        if (e == cudaSuccess) e = cudaMemset(p->d_attn_a, 0, 2 * (size_t)g.npad * qd * 2);
+        if (e == cudaSuccess) e = cudaMemset(p->d_h_a, 0, 2 * (size_t)g.npad * I * 2);
+    }
     if (e == cudaSuccess) e = cudaMemset(p->d_ctl, 0, (size_t)p->cl.total * sizeof(uint32_t));
     if (e == cudaSuccess) e = launch_rope_table(p->d_rope, c.max_seq, c.head_dim, c.rope_theta, 0);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -323,6 +412,26 @@ mk_status mk_plan_create_ex(const mk_model_cfg *cfg, const mk_weight_ptrs *w, co
     k.timeout_ns = (uint64_t)p->opt.timeout_ms * 1000000ull;
     k.trace = p->d_trace;
     k.trace_stride = p->trace_stride;
+    k.tc = g.tc ? 1 : 0;
+    k.num_ctas = g.num_ctas;
+    if (g.tc) {
+        k.npad = g.npad;
+        k.idesc = umma_idesc_bf16(kTcTileM, 2 * g.npad);
+        k.h_tiles = g.h_tiles;
+        k.aslot_bytes = g.aslot_bytes;
+        k.num_aslots = g.num_aslots;
+        uint32_t cols = 32;
+        while (cols < (uint32_t)(8 * g.npad)) cols <<= 1;  // two buffers x (gate, up) x 2 * npad columns
+        k.tmem_cols = cols;
+        for (int i = 0; i < OP_COUNT; ++i) k.tcg[i] = g.tcg[i];
+        k.tmaps = p->d_tmaps;
+        k.xa = p->d_xa;
+        k.ssq = p->d_ssq;
+        k.attn_a = p->d_attn_a;
+        k.h_a = p->d_h_a;
+        k.part = p->d_tc_part;
+        k.tile_ctr = p->d_ctl + p->cl.tile_idx;
+    }
     *out = p;
     return MK_OK;
 }
@@ -350,6 +459,12 @@ mk_status mk_decode_step_ablation(mk_plan *p, const int32_t *tokens, const int32
     KParams k = step_params(p, tokens, 1, positions, 1, kv, logits);
     if ((st = clear_trace(p, s)) != MK_OK) return st;
     static const int kOps[] = {OP_QKV, OP_ATTN, OP_O, OP_GU, OP_DOWN};
+    if (p->tables.g.tc) {
+        k.only_op = OP_EMBED;
+        k.only_layer = 0;
+        st = cuda_status(launch_megakernel(k, p->variant, p->tables.g.num_ctas, p->smem, false, s));
+        if (st != MK_OK) return st;
+    }
     for (int l = 0; l < p->cfg.n_layers; ++l)
         for (int op : kOps) {
             k.only_op = op;

@@ -55,21 +55,110 @@ struct SmemCtl {
     float red[2][kComputeWarps][8];
     float rms_part[kComputeWarps];
     float att_m[kMaxGroup], att_l[kMaxGroup], att_alpha[kMaxGroup];
+    float att_inv_l[kMaxGroup];
+    float merge_w[kMaxSplits][kMaxGroup];  // split weights exp(m_s - max_s m_s) of the merge
+    float resid[kMaxResid];                // residual rows of an O / down task, read at task start
     alignas(16) float q_s[kMaxGroup][kMaxHeadDim];
     alignas(16) float s_s[kMaxGroup][kMaxTps];
     alignas(16) uint16_t knew[kMaxHeadDim];
     alignas(16) uint16_t vnew[kMaxHeadDim];
+    // batched (tensor-core) path
+    uint64_t afull[kMaxASlots];   // activation ring
+    uint64_t aempty[kMaxASlots];
+    uint64_t acc_full[2];         // TMEM accumulator buffers: MMA issuer -> epilogue
+    uint64_t acc_empty[2];        // epilogue -> MMA issuer
+    uint64_t mma_done;            // drain of the MMA pipe at exit
+    uint32_t tmem_base;
+    uint32_t ep_last;             // the epilogue finishes this row tile (last contributor)
+    float rs[kTcMaxBatch];        // 1/rms of each sequence's projection input
+    float ssq_red[4][kTcMaxBatch];  // per-epilogue-warp partial sums of x^2
 };
 
-constexpr size_t kRingOffset = (sizeof(SmemCtl) + 1023) / 1024 * 1024;
+// The rings start at the first 1024-byte boundary after the control block
+// (the 128-byte-swizzled TMA tiles of the batched path need that alignment);
+// kRingOffset budgets for the worst placement of the dynamic window.
+constexpr size_t kRingOffset = (sizeof(SmemCtl) + 1023) / 1024 * 1024 + 1024;
 constexpr uint32_t kReadyAbort = 0x7FFFFFFFu;
 
 struct Ctx {
     const KParams *p;
     SmemCtl *sc;
-    uint8_t *ring;
+    uint8_t *ring;   // weight / KV ring
+    uint8_t *aring;  // activation ring (batched path)
     int cta;
 };
+
+__device__ __forceinline__ bool is_proj(int op) { return op == OP_QKV || op == OP_O || op == OP_GU || op == OP_DOWN || op == OP_LM; }
+
+// ------------------------------------------------------ batched-path tiles
+// Tensor maps (128 bytes each): per layer wq, wk, wv, wo, w_gate, w_up,
+// w_down; then the LM head and the three activation operands.
+constexpr int kTmPerLayer = 7;
+enum TmIdx : int { TM_WQ = 0, TM_WK, TM_WV, TM_WO, TM_WG, TM_WU, TM_WD };
+
+__device__ __forceinline__ const void *tmap(const KParams &p, int idx) { return p.tmaps + (size_t)idx * 128; }
+__device__ __forceinline__ int tm_lm(const KParams &p) { return p.L * kTmPerLayer; }
+__device__ __forceinline__ int tm_xa(const KParams &p) { return p.L * kTmPerLayer + 1; }
+__device__ __forceinline__ int tm_attn(const KParams &p) { return p.L * kTmPerLayer + 2; }
+__device__ __forceinline__ int tm_h(const KParams &p) { return p.L * kTmPerLayer + 3; }
+
+// Activation operand (tensor map) of a projection.
+__device__ __forceinline__ int act_map(const KParams &p, int op) {
+    return op == OP_O ? tm_attn(p) : (op == OP_DOWN ? tm_h(p) : tm_xa(p));
+}
+
+// Weight tensor map and local row tile of row tile `tile` of a projection
+// (matrix m = 1 is w_up of gate/up).
+__device__ __forceinline__ int weight_map(const KParams &p, int op, int layer, int tile, int m, int *ltile) {
+    *ltile = tile;
+    switch (op) {
+        case OP_QKV: {
+            const TcGeom &g = p.tcg[OP_QKV];
+            if (tile < g.tiles_q) return layer * kTmPerLayer + TM_WQ;
+            if (tile < g.tiles_q + g.tiles_k) {
+                *ltile = tile - g.tiles_q;
+                return layer * kTmPerLayer + TM_WK;
+            }
+            *ltile = tile - g.tiles_q - g.tiles_k;
+            return layer * kTmPerLayer + TM_WV;
+        }
+        case OP_O: return layer * kTmPerLayer + TM_WO;
+        case OP_GU: return layer * kTmPerLayer + (m ? TM_WU : TM_WG);
+        case OP_DOWN: return layer * kTmPerLayer + TM_WD;
+        default: return tm_lm(p);
+    }
+}
+
+// Which range (0 .. num_ctas-1) owns unit u when `units` units are cut into
+// num_ctas balanced contiguous ranges [c*U/N, (c+1)*U/N).
+__device__ __forceinline__ int32_t range_of(int64_t u, int64_t units, int64_t n) {
+    return (int32_t)(((u + 1) * n - 1) / units);
+}
+__device__ __forceinline__ int64_t range_start(int64_t c, int64_t units, int64_t n) { return c * units / n; }
+// With fewer units than ranges some ranges are empty (and have no task).
+__device__ __forceinline__ bool range_nonempty(int64_t c, int64_t units, int64_t n) {
+    return range_start(c + 1, units, n) > range_start(c, units, n);
+}
+
+// Split-bf16 activation operand [2 * npad][K]: row b holds bf16(v), row
+// npad + b holds bf16(v - bf16(v)).  One MMA with N = 2 * npad multiplies
+// both halves; their sum keeps about 16 significant bits of v.
+__device__ __forceinline__ void store_split(uint16_t *buf, int32_t K, int32_t npad, int32_t b, int64_t col, float v) {
+    const uint16_t hi = f32_to_bf16_bits(v);
+    const uint16_t lo = f32_to_bf16_bits(v - __uint_as_float((uint32_t)hi << 16));
+    buf[(int64_t)b * K + col] = hi;
+    buf[(int64_t)(npad + b) * K + col] = lo;
+}
+
+// 16 columns of a split accumulator: the high-part columns at `taddr` plus
+// the low-part columns npad further on.
+__device__ __forceinline__ void tmem_ld_split16(uint32_t taddr, int32_t npad, float (&v)[16]) {
+    float lo[16];
+    tmem_ld16(taddr, v);
+    tmem_ld16(taddr + (uint32_t)npad, lo);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] += lo[i];
+}
 
 __device__ __forceinline__ bool task_active(const KParams &p, const Task &t) {
     if (p.only_op >= 0) return t.op == p.only_op && t.layer == p.only_layer;
@@ -262,6 +351,28 @@ struct Producer {
         return true;
     }
 
+    // Batched path: one 128 x 64 weight tile per slot by TMA (two for
+    // gate/up: the gate tile, then the matching up tile).
+    __device__ bool run_gemm(const Ctx &c, const Task &t) {
+        const KParams &p = *c.p;
+        const TcGeom &g = p.tcg[t.op];
+        const int mats = (t.op == OP_GU) ? 2 : 1;
+        for (int32_t u = t.a0; u < t.a1; ++u) {
+            const int32_t tile = u / g.kchunks, kc = u % g.kchunks;
+            for (int m = 0; m < mats; ++m) {
+                uint32_t s;
+                if (!acquire_slot(c, &s)) return false;
+                int lt;
+                const int map = weight_map(p, t.op, t.layer, tile, m, &lt);
+                mbar_arrive_expect_tx(&c.sc->full[s], (uint32_t)p.slot_bytes);
+                tma_load_2d(c.ring + (size_t)s * p.slot_bytes, tmap(p, map), kc * kTcTileK, lt * kTcTileM,
+                            &c.sc->full[s], pol);
+                ++issued;
+            }
+        }
+        return true;
+    }
+
     // Wait for the copies of every slot's most recent page (abort path and
     // normal exit alike), so that no copy is in flight when the CTA exits.
     __device__ void drain(const Ctx &c) {
@@ -289,7 +400,10 @@ __device__ void producer_role(const Ctx &c, const Task *q, int nt) {
         const Task t = q[i];
         if (!task_active(*c.p, t)) continue;
         pr.tr = trace_slot(*c.p, i);
-        const bool ok = (t.op == OP_ATTN) ? pr.run_attn(c, t) : pr.run_matvec(c, t);
+        bool ok = true;
+        if (t.op == OP_ATTN) ok = pr.run_attn(c, t);
+        else if (t.op == OP_EMBED) ok = true;
+        else ok = c.p->tc ? pr.run_gemm(c, t) : pr.run_matvec(c, t);
         if (!ok) break;
     }
     pr.drain(c);
@@ -297,8 +411,47 @@ __device__ void producer_role(const Ctx &c, const Task *q, int nt) {
 
 // ------------------------------------------------------------ scheduler
 
-__device__ void scheduler_role(const Ctx &c, const Task *q, int nt) {
-    if ((threadIdx.x & 31) != 0) return;
+// Batched path: after a projection task's event fires, the scheduler streams
+// its activation operand (npad rows x 64 columns per unit, bf16, written
+// earlier in this launch by other CTAs) into the activation ring.
+struct ActProducer {
+    uint32_t issued = 0;
+    uint64_t pol;
+
+    __device__ bool run(const Ctx &c, const Task &t) {
+        const KParams &p = *c.p;
+        const TcGeom &g = p.tcg[t.op];
+        const void *map = tmap(p, act_map(p, t.op));
+        const uint32_t ns = (uint32_t)p.num_aslots;
+        fence_proxy_async_global();  // generic-proxy writes (ordered by the acquire) -> TMA reads
+        for (int32_t u = t.a0; u < t.a1; ++u) {
+            const uint32_t s = issued % ns, round = issued / ns;
+            if (!wait_mbar(c, &c.sc->aempty[s], (round & 1u) ^ 1u, SITE_EMPTY_WAIT)) return false;
+            mbar_arrive_expect_tx(&c.sc->afull[s], (uint32_t)p.aslot_bytes);
+            tma_load_2d(c.aring + (size_t)s * p.aslot_bytes, map, (u % g.kchunks) * kTcTileK, 0, &c.sc->afull[s], pol);
+            ++issued;
+        }
+        return true;
+    }
+
+    __device__ void drain(const Ctx &c) {
+        const uint32_t ns = (uint32_t)c.p->num_aslots;
+        const uint32_t lim = issued < ns ? issued : ns;
+        for (uint32_t s = 0; s < lim; ++s) {
+            const uint32_t k = issued - 1 - ((issued - 1 - s) % ns);
+            const uint32_t par = (k / ns) & 1u;
+            uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(&c.sc->afull[s], par)) {
+                if (globaltimer_ns() - t0 > c.p->timeout_ns) {
+                    record_error(c, 4, SITE_DRAIN_WAIT, (int32_t)s);
+                    break;
+                }
+            }
+        }
+    }
+};
+
+__device__ void scheduler_loop(const Ctx &c, const Task *q, int nt, ActProducer &ap) {
     const KParams &p = *c.p;
     const bool use_events = p.only_op < 0;
     for (int i = 0; i < nt; ++i) {
@@ -326,7 +479,19 @@ __device__ void scheduler_role(const Ctx &c, const Task *q, int nt) {
         }
         if (uint64_t *tr = trace_slot(p, i)) tr[0] = globaltimer_ns();
         st_release_cta(&c.sc->ready, (uint32_t)(i + 1));
+        if (p.tc && is_proj(t.op) && task_active(p, t) && !ap.run(c, t)) {
+            st_release_cta(&c.sc->ready, kReadyAbort);
+            return;
+        }
     }
+}
+
+__device__ void scheduler_role(const Ctx &c, const Task *q, int nt) {
+    if ((threadIdx.x & 31) != 0) return;
+    ActProducer ap;
+    ap.pol = policy_evict_last();
+    scheduler_loop(c, q, nt, ap);
+    if (c.p->tc) ap.drain(c);
 }
 
 // --------------------------------------------------------- compute warps
@@ -344,6 +509,54 @@ __device__ __forceinline__ float warp_max(float v) {
 }
 
 __device__ __forceinline__ void compute_bar() { named_bar_sync(1, kComputeThreads); }
+// Barrier of the compute warps that also ORs a flag over them, so that every
+// warp takes the same branch on it.
+__device__ __forceinline__ bool compute_bar_or(bool v) { return named_bar_or(1, kComputeThreads, v); }
+// Barrier of the four epilogue warps of the batched path.
+constexpr int kEpiThreads = 128;
+__device__ __forceinline__ void epi_bar() { named_bar_sync(2, kEpiThreads); }
+
+// Sums 8 per-lane values over the warp and scatters the result: lane l
+// returns the warp total of value l/4 (each total lands on 4 lanes).  Halving
+// exchanges (16, 8, 4) then two full butterflies: 9 shuffles instead of 40.
+__device__ __forceinline__ float warp_reduce8(const float (&a)[8], int lane) {
+    const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4;
+    float b[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float send = h16 ? a[i] : a[i + 4];
+        b[i] = (h16 ? a[i + 4] : a[i]) + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
+    }
+    float c2[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float send = h8 ? b[i] : b[i + 2];
+        c2[i] = (h8 ? b[i + 2] : b[i]) + __shfl_xor_sync(0xFFFFFFFFu, send, 8);
+    }
+    float d = (h4 ? c2[1] : c2[0]) + __shfl_xor_sync(0xFFFFFFFFu, h4 ? c2[0] : c2[1], 4);
+    d += __shfl_xor_sync(0xFFFFFFFFu, d, 2);
+    d += __shfl_xor_sync(0xFFFFFFFFu, d, 1);
+    return d;
+}
+
+
+// Sums 16 per-lane values over the warp and scatters the result: lane l
+// returns the warp total of value (l / 2) % 16 (each total lands on 2 lanes).
+__device__ __forceinline__ float warp_reduce16(const float (&a)[16], int lane) {
+    const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4, h2 = lane & 2;
+    float b[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) b[i] = (h16 ? a[i + 8] : a[i]) + __shfl_xor_sync(0xFFFFFFFFu, h16 ? a[i] : a[i + 8], 16);
+    float c4[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c4[i] = (h8 ? b[i + 4] : b[i]) + __shfl_xor_sync(0xFFFFFFFFu, h8 ? b[i] : b[i + 4], 8);
+    float d2[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) d2[i] = (h4 ? c4[i + 2] : c4[i]) + __shfl_xor_sync(0xFFFFFFFFu, h4 ? c4[i] : c4[i + 2], 4);
+    float e = (h2 ? d2[1] : d2[0]) + __shfl_xor_sync(0xFFFFFFFFu, h2 ? d2[0] : d2[1], 2);
+    e += __shfl_xor_sync(0xFFFFFFFFu, e, 1);
+    return e;
+}
 
 __device__ __forceinline__ float dot8(const uint4 w, const float *x) {
     float a = bf16_lo(w.x) * x[0];
@@ -358,7 +571,9 @@ __device__ __forceinline__ float dot8(const uint4 w, const float *x) {
 }
 
 struct Consumer {
-    uint32_t consumed = 0;
+    uint32_t consumed = 0;   // weight / KV ring slots
+    uint32_t aconsumed = 0;  // activation ring slots (batched path)
+    uint32_t seg = 0;        // accumulator segments (batched path)
     int ct, wc, lane;  // compute-thread index, compute-warp index, lane
     uint32_t red_buf = 0;
     bool tracing = false;
@@ -376,13 +591,25 @@ struct Consumer {
         return s;
     }
 
+    // Batch 1: one arrival per compute warp.  Batched path: the slot's empty
+    // barrier also takes MMA commits, so it counts one arrival, made after
+    // every compute warp is done with the slot.
     __device__ void release_slot(const Ctx &c, uint32_t s) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&c.sc->empty[s]);
+        if (c.p->tc) {
+            compute_bar();
+            if (ct == 0) mbar_arrive(&c.sc->empty[s]);
+        } else {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&c.sc->empty[s]);
+        }
         ++consumed;
     }
 
     // ------------------------------------------------------- matvec task
+    // Thread ct owns input chunks ct + 256 j (8 columns each), which are
+    // exactly its chunk of row piece j; so every slot costs each thread one
+    // 128-bit shared load and 8 FMAs per row.  Row sums are kept per thread
+    // across the pieces of a row group and reduced once per group.
     template <int MAXCH>
     __device__ void run_matvec(const Ctx &c, const Task &t) {
         const KParams &p = *c.p;
@@ -391,8 +618,18 @@ struct Consumer {
         const int32_t nchunk = g.K / 8;
         const LayerW &lw = p.layers[t.layer];
         const int32_t token = p.tokens[0];
+        const bool has_resid = (op == OP_O || op == OP_DOWN);
+        const int32_t nrows = t.a1 - t.a0;
+        const bool resid_in_smem = has_resid && nrows <= kMaxResid;
+        if (resid_in_smem) {
+            // residual rows of this task, read once up front (ordered by the first group's barrier)
+            for (int32_t i = ct; i < nrows; i += kComputeThreads)
+                c.sc->resid[i] = (op == OP_O && t.layer == 0)
+                                     ? __uint_as_float((uint32_t)p.embed[(int64_t)token * p.H + t.a0 + i] << 16)
+                                     : __ldcg(p.x + t.a0 + i);
+        }
 
-        // input vector for this thread's chunks c = ct + 256 j
+        // input vector for this thread's chunks
         float xr[MAXCH][8];
         const bool from_embed = (op == OP_QKV && t.layer == 0);
         const float *xin = (op == OP_O) ? p.attn_out : (op == OP_DOWN ? p.hbuf : p.x);
@@ -444,37 +681,31 @@ struct Consumer {
             }
         }
 
+        const int lq = lane >> 2;  // row this lane holds after the reduce-scatter
         for (int32_t row = t.a0; row < t.a1;) {
             const int32_t n = mv_group_rows(p, op, row, t.a1);
             const int32_t R = n * g.row_mult;
             float acc[8];
 #pragma unroll
             for (int r = 0; r < 8; ++r) acc[r] = 0.f;
-            for (int32_t ks = 0; ks < g.ksplit; ++ks) {
-                const uint32_t s = wait_slot(c);
-                const int32_t c_lo = ks * (g.kc / 8);
-                const int32_t pw8 = min(g.kc / 8, nchunk - c_lo);  // chunks in this piece
-                const uint4 *base = reinterpret_cast<const uint4 *>(c.ring + (size_t)s * p.slot_bytes);
 #pragma unroll
-                for (int j = 0; j < MAXCH; ++j) {
-                    const int32_t cl = ct + kComputeThreads * j - c_lo;
-                    if (cl >= 0 && cl < pw8) {
+            for (int ks = 0; ks < MAXCH; ++ks) {
+                if (ks < g.ksplit) {
+                    const uint32_t s = wait_slot(c);
+                    const int32_t pw8 = min(g.kc, g.K - ks * g.kc) >> 3;  // chunks per row in this piece
+                    const uint4 *base = reinterpret_cast<const uint4 *>(c.ring + (size_t)s * p.slot_bytes) + ct;
+                    // the slot goes back to the producer as soon as its data is in registers
+                    uint4 w[8];
 #pragma unroll
-                        for (int r = 0; r < 8; ++r) {
-                            if (r < R) acc[r] += dot8(base[r * pw8 + cl], xr[j]);
-                        }
-                    }
-                }
-                release_slot(c, s);
-            }
-            // reduce the R row sums over the 256 compute threads
+                    for (int r = 0; r < 8; ++r) w[r] = (ct < pw8 && r < R) ? base[r * pw8] : make_uint4(0u, 0u, 0u, 0u);
+                    release_slot(c, s);
 #pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                if (r < R) {
-                    const float v = warp_sum(acc[r]);
-                    if (lane == 0) c.sc->red[red_buf][wc][r] = v;
+                    for (int r = 0; r < 8; ++r) acc[r] += dot8(w[r], xr[ks]);
                 }
             }
+            // reduce-scatter of the 8 row sums over the warp: lane l ends with row l/4
+            const float v = warp_reduce8(acc, lane);
+            if ((lane & 3) == 0) c.sc->red[red_buf][wc][lq] = v;
             compute_bar();
             if (ct < n) {
                 float tot = 0.f, tot2 = 0.f;
@@ -485,22 +716,278 @@ struct Consumer {
                     for (int w = 0; w < kComputeWarps; ++w) tot2 += c.sc->red[red_buf][w][n + ct];
                 }
                 const int32_t orow = row + ct;
+                float xo = 0.f;
+                if (has_resid) {
+                    xo = resid_in_smem ? c.sc->resid[orow - t.a0]
+                                       : ((op == OP_O && t.layer == 0)
+                                              ? __uint_as_float((uint32_t)p.embed[(int64_t)token * p.H + orow] << 16)
+                                              : __ldcg(p.x + orow));
+                }
                 switch (op) {
                     case OP_QKV: p.qkv[orow] = tot; break;
-                    case OP_O: {
-                        const float xo = (t.layer == 0)
-                                             ? __uint_as_float((uint32_t)p.embed[(int64_t)token * p.H + orow] << 16)
-                                             : __ldcg(p.x + orow);
-                        p.x[orow] = xo + tot;
-                        break;
-                    }
+                    case OP_O:
+                    case OP_DOWN: p.x[orow] = xo + tot; break;
                     case OP_GU: p.hbuf[orow] = tot / (1.f + expf(-tot)) * tot2; break;
-                    case OP_DOWN: p.x[orow] = __ldcg(p.x + orow) + tot; break;
                     default: p.logits[orow] = tot; break;
                 }
             }
             red_buf ^= 1u;
             row += n;
+        }
+    }
+
+    // ------------------------------------------ batched path: projections
+    // Units [a0, a1) of the operator, cut by row tile into segments.  Compute
+    // warp 0, lane 0 issues the MMAs of each segment into one of two TMEM
+    // accumulator buffers; compute warps 2..5 (TMEM lane quarters 0..3) read
+    // them back and run the fused epilogue; the other compute warps idle.
+    __device__ void run_gemm(const Ctx &c, const Task &t) {
+        const KParams &p = *c.p;
+        const TcGeom &g = p.tcg[t.op];
+        const int mats = (t.op == OP_GU) ? 2 : 1;
+        const int32_t t0 = t.a0 / g.kchunks, t1 = (t.a1 - 1) / g.kchunks;
+        const bool issuer = (wc == 0 && lane == 0);
+        if (issuer) mma_issuer(c, t, g, mats, t0, t1);
+        else if (wc >= 2 && wc < 6) epilogue(c, t, g, mats, t0, t1);
+        if (!issuer) {
+            consumed += (uint32_t)((t.a1 - t.a0) * mats);
+            aconsumed += (uint32_t)(t.a1 - t.a0);
+        }
+        seg += (uint32_t)(t1 - t0 + 1);
+    }
+
+    __device__ void mma_issuer(const Ctx &c, const Task &t, const TcGeom &g, int mats, int32_t t0, int32_t t1) {
+        const KParams &p = *c.p;
+        SmemCtl *sc = c.sc;
+        const uint32_t ns = (uint32_t)p.num_slots, nas = (uint32_t)p.num_aslots;
+        uint32_t sg = seg;
+        for (int32_t tile = t0; tile <= t1; ++tile, ++sg) {
+            const int32_t klo = (tile == t0) ? t.a0 % g.kchunks : 0;
+            const int32_t khi = (tile == t1) ? (t.a1 - 1) % g.kchunks + 1 : g.kchunks;
+            const uint32_t ab = sg & 1u, use = sg >> 1;
+            if (!wait_mbar(c, &sc->acc_empty[ab], (use & 1u) ^ 1u, SITE_ACC_WAIT)) return;
+            tc_fence_after();
+            const uint32_t dcol = sc->tmem_base + ab * 4u * (uint32_t)p.npad;
+            for (int32_t k = klo; k < khi; ++k) {
+                uint32_t ws[2] = {0u, 0u};
+                for (int m = 0; m < mats; ++m) {
+                    ws[m] = consumed % ns;
+                    if (!wait_mbar(c, &sc->full[ws[m]], (consumed / ns) & 1u, SITE_FULL_WAIT)) return;
+                    ++consumed;
+                }
+                const uint32_t as = aconsumed % nas;
+                if (!wait_mbar(c, &sc->afull[as], (aconsumed / nas) & 1u, SITE_FULL_WAIT)) return;
+                ++aconsumed;
+                tc_fence_after();
+                const uint32_t abase = smem_u32(c.aring + (size_t)as * p.aslot_bytes);
+                for (int m = 0; m < mats; ++m) {
+                    const uint32_t wbase = smem_u32(c.ring + (size_t)ws[m] * p.slot_bytes);
+#pragma unroll
+                    for (int kk = 0; kk < kTcTileK / 16; ++kk)
+                        umma_bf16(dcol + (uint32_t)(m * 2 * p.npad), umma_desc_sw128(wbase + kk * 32),
+                                  umma_desc_sw128(abase + kk * 32), p.idesc, (k > klo || kk > 0) ? 1u : 0u);
+                }
+                for (int m = 0; m < mats; ++m) umma_commit(&sc->empty[ws[m]]);
+                umma_commit(&sc->aempty[as]);
+            }
+            umma_commit(&sc->acc_full[ab]);
+        }
+    }
+
+    // Epilogue warps: for each segment, wait for its accumulator, publish or
+    // gather the partial sums of a shared row tile, and finish the tile.
+    __device__ void epilogue(const Ctx &c, const Task &t, const TcGeom &g, int mats, int32_t t0, int32_t t1) {
+        const KParams &p = *c.p;
+        SmemCtl *sc = c.sc;
+        const int op = t.op;
+        const int q4 = (wc + 2) & 3;  // TMEM lane quarter of this warp (its warp id mod 4)
+        const int r = q4 * 32 + lane; // row of the tile held by this thread
+        const int et = ct - 64;       // 0..127
+        if (op == OP_QKV || op == OP_GU || op == OP_LM) {
+            // RMSNorm scale of each sequence from the producers' per-tile sums of x^2
+            for (int b = et; b < p.B; b += kEpiThreads) {
+                float ssum = 0.f;
+                for (int j = 0; j < p.h_tiles; ++j) ssum += __ldcg(p.ssq + (size_t)b * p.h_tiles + j);
+                sc->rs[b] = rsqrtf(ssum / (float)p.H + p.eps);
+            }
+        }
+        epi_bar();
+        const int64_t U = g.units, NR = p.num_ctas;
+        const int32_t rc = t.a2;  // this task's range number
+        uint32_t sg = seg;
+        for (int32_t tile = t0; tile <= t1; ++tile, ++sg) {
+            const int32_t klo = (tile == t0) ? t.a0 % g.kchunks : 0;
+            const int32_t khi = (tile == t1) ? (t.a1 - 1) % g.kchunks + 1 : g.kchunks;
+            const uint32_t ab = sg & 1u, use = sg >> 1;
+            wait_mbar(c, &sc->acc_full[ab], use & 1u, SITE_ACC_WAIT);
+            tc_fence_after();
+            const uint32_t tq = sc->tmem_base + ((uint32_t)(q4 * 32) << 16) + ab * 4u * (uint32_t)p.npad;
+            const bool whole = (klo == 0 && khi == g.kchunks);
+            int32_t cf = rc, cl = rc;
+            bool last = true;
+            if (!whole) {
+                // several ranges share this row tile: publish this partial sum,
+                // the last range to arrive adds them all up in range order
+                const int64_t tu0 = (int64_t)tile * g.kchunks;
+                cf = range_of(tu0, U, NR);
+                cl = range_of(tu0 + g.kchunks - 1, U, NR);
+                float *mine = part_ptr(p, rc, tile, g);
+                for (int m = 0; m < mats; ++m)
+                    for (int c0 = 0; c0 < p.npad; c0 += 16) {
+                        float v[16];
+                        tmem_ld_split16(tq + (uint32_t)(m * 2 * p.npad + c0), p.npad, v);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) __stcg(mine + ((size_t)m * p.npad + c0 + i) * kTcTileM + r, v[i]);
+                    }
+                __threadfence();
+                epi_bar();
+                if (et == 0) {
+                    uint32_t n_contrib = 0;  // non-empty ranges meeting this tile
+                    for (int32_t cc = cf; cc <= cl; ++cc) n_contrib += range_nonempty(cc, U, NR) ? 1u : 0u;
+                    uint32_t *ctr = p.tile_ctr + g.ctr_off + tile;
+                    const uint32_t old = atom_acq_rel_gpu_add(ctr, 1u);
+                    const bool l = (old + 1u == n_contrib);
+                    if (l) *ctr = 0u;  // every range of this tile has arrived; ready for the next use
+                    sc->ep_last = l ? 1u : 0u;
+                }
+                epi_bar();
+                last = sc->ep_last != 0u;
+            }
+            if (last) finish_tile(c, t, g, mats, tile, r, tq, whole, cf, cl, rc);
+            tc_fence_before();
+            epi_bar();
+            if (et == 0) mbar_arrive(&sc->acc_empty[ab]);
+        }
+    }
+
+    // Partial-sum slot [2][npad][128] of range rc for row tile `tile`: slot 0
+    // when the tile is the range's first, else slot 1 (its last).
+    __device__ static float *part_ptr(const KParams &p, int32_t rc, int32_t tile, const TcGeom &g) {
+        const int64_t first_tile = range_start(rc, g.units, p.num_ctas) / g.kchunks;
+        const int sidx = (first_tile == tile) ? 0 : 1;
+        return p.part + ((size_t)rc * 2 + sidx) * 2 * (size_t)p.npad * kTcTileM;
+    }
+
+    __device__ void finish_tile(const Ctx &c, const Task &t, const TcGeom &g, int mats, int32_t tile, int r,
+                                uint32_t tq, bool whole, int32_t cf, int32_t cl, int32_t rc) {
+        const KParams &p = *c.p;
+        SmemCtl *sc = c.sc;
+        const int op = t.op;
+        const int q4 = (wc + 2) & 3;
+        const int et = ct - 64;
+        // where this thread's row goes
+        int32_t orow = tile * kTcTileM + r, obase = 0, olim = g.rows;
+        if (op == OP_QKV) {
+            const int32_t qr = p.nq * p.d, kr = p.nkv * p.d;
+            if (tile < g.tiles_q) {
+                olim = qr;
+            } else if (tile < g.tiles_q + g.tiles_k) {
+                orow = (tile - g.tiles_q) * kTcTileM + r;
+                obase = qr;
+                olim = kr;
+            } else {
+                orow = (tile - g.tiles_q - g.tiles_k) * kTcTileM + r;
+                obase = qr + kr;
+                olim = kr;
+            }
+        }
+        const bool row_ok = orow < olim;
+        float gain = 0.f;
+        if ((op == OP_O || op == OP_DOWN) && row_ok) {
+            const uint16_t *gv = (op == OP_O) ? p.layers[t.layer].mlp_norm
+                                              : (t.layer + 1 < p.L ? p.layers[t.layer + 1].attn_norm : p.final_norm);
+            gain = __uint_as_float((uint32_t)gv[orow] << 16);
+        }
+        for (int c0 = 0; c0 < p.npad; c0 += 16) {
+            float v[2][16];
+            for (int m = 0; m < mats; ++m) {
+                if (whole) {
+                    tmem_ld_split16(tq + (uint32_t)(m * 2 * p.npad + c0), p.npad, v[m]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[m][i] = 0.f;
+                    for (int32_t cc = cf; cc <= cl; ++cc) {
+                        if (!range_nonempty(cc, g.units, p.num_ctas)) continue;
+                        float w[16];
+                        if (cc == rc) {
+                            tmem_ld_split16(tq + (uint32_t)(m * 2 * p.npad + c0), p.npad, w);
+                        } else {
+                            const float *src = part_ptr(p, cc, tile, g) + ((size_t)m * p.npad + c0) * kTcTileM + r;
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) w[i] = __ldcg(src + (size_t)i * kTcTileM);
+                        }
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[m][i] += w[i];
+                    }
+                }
+            }
+            float sq[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                sq[i] = 0.f;
+                const int b = c0 + i;
+                if (b >= p.B || !row_ok) continue;
+                switch (op) {
+                    case OP_QKV: p.qkv[(size_t)b * p.qkv_rows + obase + orow] = sc->rs[b] * v[0][i]; break;
+                    case OP_O:
+                    case OP_DOWN: {
+                        const size_t xi = (size_t)b * p.H + orow;
+                        const float xn = __ldcg(p.x + xi) + v[0][i];
+                        p.x[xi] = xn;
+                        store_split(p.xa, p.H, p.npad, b, orow, gain * xn);
+                        sq[i] = xn * xn;
+                        break;
+                    }
+                    case OP_GU: {
+                        const float gg = sc->rs[b] * v[0][i], uu = sc->rs[b] * v[1][i];
+                        store_split(p.h_a, p.I, p.npad, b, orow, gg / (1.f + expf(-gg)) * uu);
+                        break;
+                    }
+                    default: p.logits[(size_t)b * p.V + orow] = sc->rs[b] * v[0][i]; break;
+                }
+            }
+            if (op == OP_O || op == OP_DOWN) {
+                // per-warp sums of x^2 for the 16 sequences of this chunk
+                const float s16 = warp_reduce16(sq, lane);
+                if ((lane & 1) == 0) sc->ssq_red[q4][c0 + ((lane >> 1) & 15)] = s16;
+            }
+        }
+        if (op == OP_O || op == OP_DOWN) {
+            epi_bar();
+            for (int b = et; b < p.B; b += kEpiThreads)
+                p.ssq[(size_t)b * p.h_tiles + tile] =
+                    sc->ssq_red[0][b] + sc->ssq_red[1][b] + sc->ssq_red[2][b] + sc->ssq_red[3][b];
+        }
+    }
+
+    // ------------------------------------------ batched path: embedding
+    // Items [a0, a1) = (sequence, 128-row tile of H): x = embed[token],
+    // xa = bf16(attn_norm_0 * x), and the tile's sum of x^2.
+    __device__ void run_embed(const Ctx &c, const Task &t) {
+        const KParams &p = *c.p;
+        const uint16_t *gain = p.layers[0].attn_norm;
+        for (int32_t it = t.a0; it < t.a1; ++it) {
+            const int32_t b = it / p.h_tiles, j = it % p.h_tiles;
+            const int32_t tok = p.tokens[(int64_t)b * p.tok_stride];
+            float sq = 0.f;
+            const int32_t row = j * kTcTileM + ct;
+            if (ct < kTcTileM && row < p.H) {
+                const float e = __uint_as_float((uint32_t)p.embed[(int64_t)tok * p.H + row] << 16);
+                const size_t xi = (size_t)b * p.H + row;
+                p.x[xi] = e;
+                store_split(p.xa, p.H, p.npad, b, row, __uint_as_float((uint32_t)gain[row] << 16) * e);
+                sq = e * e;
+            }
+            sq = warp_sum(sq);
+            if (lane == 0) c.sc->rms_part[wc] = sq;
+            compute_bar();
+            if (ct == 0) {
+                float tot = 0.f;
+#pragma unroll
+                for (int w = 0; w < kComputeWarps; ++w) tot += c.sc->rms_part[w];
+                p.ssq[(size_t)b * p.h_tiles + j] = tot;
+            }
+            compute_bar();
         }
     }
 
@@ -684,31 +1171,57 @@ struct Consumer {
         }
         compute_bar();
         if (sc->last_flag) {
-            // last split of this (sequence, kv head): merge the S partials
+            // last split of this (sequence, kv head): merge the S partials.
+            // Split weights exp(m_s - M) and 1/L first, then every thread
+            // sums its output pairs over the splits with independent loads.
             if (ct == 0) *done = 0u;  // nothing else touches it in this launch
             const int64_t pbase = ((int64_t)b * p.nkv + kvh) * S * G;
+            if (wc < G) {
+                const int g = wc;
+                float M = -INFINITY;
+                for (int s = lane; s < S; s += 32)
+                    M = fmaxf(M, __ldcg(p.attn_part + (pbase + (int64_t)s * G + g) * (d + 2) + d));
+                M = warp_max(M);
+                float Ls = 0.f;
+                for (int s = lane; s < S; s += 32) {
+                    const float *src = p.attn_part + (pbase + (int64_t)s * G + g) * (d + 2);
+                    const float ms = __ldcg(src + d);
+                    const float w = (ms == -INFINITY) ? 0.f : expf(ms - M);
+                    sc->merge_w[s][g] = w;
+                    Ls = fmaf(__ldcg(src + d + 1), w, Ls);
+                }
+                Ls = warp_sum(Ls);
+                if (lane == 0) sc->att_inv_l[g] = 1.f / Ls;
+            }
+            compute_bar();
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
                 if (k < mine) {
                     const int pr = ct + kComputeThreads * k;
                     const int g = pr / half, e = (pr % half) * 2;
-                    float M = -INFINITY;
-                    for (int s = 0; s < S; ++s)
-                        M = fmaxf(M, __ldcg(p.attn_part + (pbase + (int64_t)s * G + g) * (d + 2) + d));
-                    float Ls = 0.f, o0 = 0.f, o1 = 0.f;
+                    const float *src = p.attn_part + (pbase + g) * (d + 2) + e;
+                    const int64_t sstride = (int64_t)G * (d + 2);
+                    float o0 = 0.f, o1 = 0.f;
+#pragma unroll 8
                     for (int s = 0; s < S; ++s) {
-                        const float *src = p.attn_part + (pbase + (int64_t)s * G + g) * (d + 2);
-                        const float ms = __ldcg(src + d);
-                        const float w = (ms == -INFINITY) ? 0.f : expf(ms - M);
-                        Ls = fmaf(__ldcg(src + d + 1), w, Ls);
-                        o0 = fmaf(__ldcg(src + e), w, o0);
-                        o1 = fmaf(__ldcg(src + e + 1), w, o1);
+                        const float2 v = __ldcg(reinterpret_cast<const float2 *>(src + s * sstride));
+                        const float w = sc->merge_w[s][g];
+                        o0 = fmaf(v.x, w, o0);
+                        o1 = fmaf(v.y, w, o1);
                     }
-                    float *dst = p.attn_out + (int64_t)b * p.nq * d + (int64_t)(kvh * G + g) * d;
-                    dst[e] = o0 / Ls;
-                    dst[e + 1] = o1 / Ls;
+                    const float il = sc->att_inv_l[g];
+                    const int64_t oi = (int64_t)b * p.nq * d + (int64_t)(kvh * G + g) * d + e;
+                    if (p.tc) {
+                        // split-bf16 operand of the O projection's tensor-core tiles
+                        const int64_t col = (int64_t)(kvh * G + g) * d + e;
+                        store_split(p.attn_a, p.nq * d, p.npad, b, col, o0 * il);
+                        store_split(p.attn_a, p.nq * d, p.npad, b, col + 1, o1 * il);
+                    } else {
+                        *reinterpret_cast<float2 *>(p.attn_out + oi) = make_float2(o0 * il, o1 * il);
+                    }
                 }
             }
+            if (p.tc) fence_proxy_async_global();  // read next by the O projection's TMA
             compute_bar();
             if (ct == 0 && p.only_op < 0 && t.signal_ev != kNoEvent && !local_abort(c)) {
                 __threadfence();
@@ -743,19 +1256,22 @@ __device__ void compute_role(const Ctx &c, const Task *q, int nt) {
                 }
             }
         }
-        compute_bar();  // every compute warp sees the same abort state
-        if (local_abort(c)) return;
+        if (compute_bar_or(local_abort(c))) return;  // every compute warp takes the same branch
         uint64_t *tr = cs.tracing ? trace_slot(p, i) : nullptr;
         if (tr) tr[1] = globaltimer_ns();
         if (t.op == OP_ATTN) cs.run_attn(c, t);
+        else if (t.op == OP_EMBED) cs.run_embed(c, t);
+        else if (p.tc) cs.run_gemm(c, t);
         else cs.run_matvec<MAXCH>(c, t);
-        compute_bar();  // every output row of the task is written
+        // batched path: outputs are read by other CTAs' TMA (async proxy)
+        if (p.tc) fence_proxy_async_global();
+        const bool aborted = compute_bar_or(local_abort(c));  // every output row of the task is written
         if (tr) {
             tr[2] = globaltimer_ns();
             tr[3] = cs.full_wait_ns;
             cs.full_wait_ns = 0;
         }
-        if (local_abort(c)) return;
+        if (aborted) return;
         if (t.op != OP_ATTN && p.only_op < 0 && t.signal_ev != kNoEvent && cs.ct == 0) {
             __threadfence();
             red_release_gpu_add(p.ctl + t.signal_ev, 1u);
@@ -767,22 +1283,42 @@ template <int MAXCH>
 __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant__ KParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     SmemCtl *sc = reinterpret_cast<SmemCtl *>(smem_raw);
-    Ctx c{&p, sc, smem_raw + kRingOffset, (int)blockIdx.x};
+    const uint32_t ctl_end = smem_u32(smem_raw) + (uint32_t)sizeof(SmemCtl);
+    uint8_t *ring = smem_raw + (((ctl_end + 1023u) & ~1023u) - smem_u32(smem_raw));
+    Ctx c{&p, sc, ring, ring + (size_t)p.num_slots * p.slot_bytes, (int)blockIdx.x};
     const Task *q = p.tasks + p.queue_off[blockIdx.x];
     const int nt = p.queue_off[blockIdx.x + 1] - p.queue_off[blockIdx.x];
     const int warp = threadIdx.x >> 5;
+    constexpr int kWarpMma = 2;  // batched path: TMEM owner and MMA issuer (compute warp 0)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.num_slots; ++s) {
             mbar_init(&sc->full[s], 1);
-            mbar_init(&sc->empty[s], kComputeWarps);
+            mbar_init(&sc->empty[s], p.tc ? 1 : kComputeWarps);
+        }
+        if (p.tc) {
+            for (int s = 0; s < p.num_aslots; ++s) {
+                mbar_init(&sc->afull[s], 1);
+                mbar_init(&sc->aempty[s], 1);
+            }
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(&sc->acc_full[i], 1);
+                mbar_init(&sc->acc_empty[i], 1);
+            }
+            mbar_init(&sc->mma_done, 1);
         }
         sc->ready = 0;
         sc->abort = global_abort(p) ? 1u : 0u;  // a recorded error stays sticky
         sc->last_flag = 0;
         fence_mbar_init();
     }
+    if (p.tc && warp == kWarpMma) {
+        tmem_alloc(&sc->tmem_base, p.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
     // validate this step's inputs before any address is formed from them
     if (threadIdx.x < 32 && !sc->abort) {
         for (int b = threadIdx.x; b < p.B; b += 32) {
@@ -811,7 +1347,23 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant_
         else if (warp == kWarpProd) producer_role(c, q, nt);
         else compute_role<MAXCH>(c, q, nt);
     }
+    if (p.tc && threadIdx.x == kWarpMma * 32) {
+        // no MMA may still be reading shared memory or writing TMEM at exit
+        umma_commit(&sc->mma_done);
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(&sc->mma_done, 0)) {
+            if (globaltimer_ns() - t0 > p.timeout_ns) {
+                record_error(c, 4, SITE_DRAIN_WAIT, -1);
+                break;
+            }
+        }
+    }
+    tc_fence_before();
     __syncthreads();
+    if (p.tc && warp == kWarpMma) {
+        tc_fence_after();
+        tmem_dealloc(sc->tmem_base, p.tmem_cols);
+    }
     if (threadIdx.x == 0) {
         // the last CTA out resets the counters for the next launch
         __threadfence();
@@ -891,11 +1443,12 @@ const void *variant_ptr(int variant) {
 
 }  // namespace
 
-size_t megakernel_smem_bytes(int32_t slot_bytes, int32_t num_slots) {
-    return kRingOffset + (size_t)slot_bytes * num_slots;
+size_t megakernel_smem_bytes(int32_t slot_bytes, int32_t num_slots, int32_t aslot_bytes, int32_t num_aslots) {
+    return kRingOffset + (size_t)slot_bytes * num_slots + (size_t)aslot_bytes * num_aslots;
 }
 
-int megakernel_variant(int32_t max_k) {
+int megakernel_variant(int32_t max_k, bool tc) {
+    if (tc) return 2;  // no register-resident matvec input on the batched path
     const int nch = (max_k / 8 + kComputeThreads - 1) / kComputeThreads;
     if (nch <= 2) return 2;
     if (nch <= 4) return 4;

@@ -17,6 +17,8 @@ constexpr int kMaxSlots = 16;
 constexpr int kMaxGroup = 8;      // q heads per kv head
 constexpr int kMaxHeadDim = 128;
 constexpr int kMaxTps = 128;      // KV tokens per ring slot
+constexpr int kMaxResid = 512;    // residual rows prefetched per matvec task
+constexpr int kMaxASlots = 8;     // activation ring slots (batched path)
 
 struct KParams {
     // shape
@@ -55,13 +57,31 @@ struct KParams {
     // optional task trace: [num_ctas][trace_stride][8] globaltimer stamps
     uint64_t *trace;
     int32_t trace_stride;
+    // batched (tensor-core) path
+    int32_t tc;              // nonzero: projections run as tcgen05 tiles
+    int32_t npad;            // MMA N: batch rounded up to 16
+    uint32_t idesc;          // kind::f16 instruction descriptor (M 128, N npad)
+    int32_t num_ctas;        // ranges per projection
+    int32_t h_tiles;         // 128-row tiles of the hidden size
+    int32_t aslot_bytes, num_aslots;
+    uint32_t tmem_cols;
+    TcGeom tcg[OP_COUNT];
+    const uint8_t *tmaps;    // CUtensorMap[7 * L + 4], see the kernel's TmIdx
+    uint16_t *xa;            // bf16 [B][H]: x times the next consumer's RMSNorm gain
+    float *ssq;              // fp32 [B][h_tiles]: sums of x^2 over 128-row tiles of x
+    uint16_t *attn_a;        // bf16 [B][nq*d]: attention output
+    uint16_t *h_a;           // bf16 [B][I]: SiLU(gate) * up
+    float *part;             // fp32 [num_ctas][2][2][npad][128]: partial row-tile sums
+    uint32_t *tile_ctr;      // row-tile arrival counters
 };
 
-// Shared memory the megakernel needs for a given ring.
-size_t megakernel_smem_bytes(int32_t slot_bytes, int32_t num_slots);
+// Shared memory the megakernel needs for a given ring (plus the activation
+// ring of the batched path).
+size_t megakernel_smem_bytes(int32_t slot_bytes, int32_t num_slots, int32_t aslot_bytes, int32_t num_aslots);
 
-// Picks the register-tile variant for the longest matvec input.
-int megakernel_variant(int32_t max_k);
+// Picks the register-tile variant for the longest matvec input (batch 1), or
+// the tensor-core variant (batched).
+int megakernel_variant(int32_t max_k, bool tc);
 
 // Launches the megakernel: cooperative (persistent mode) or plain (ablation).
 cudaError_t launch_megakernel(const KParams &p, int variant, int grid, size_t smem, bool cooperative,

@@ -6,13 +6,21 @@
 
 namespace mk {
 
-enum Op : uint8_t { OP_NONE = 0, OP_QKV = 1, OP_ATTN = 2, OP_O = 3, OP_GU = 4, OP_DOWN = 5, OP_LM = 6, OP_COUNT = 7 };
+enum Op : uint8_t {
+    OP_NONE = 0, OP_QKV = 1, OP_ATTN = 2, OP_O = 3, OP_GU = 4, OP_DOWN = 5, OP_LM = 6,
+    OP_EMBED = 7,  // batched path only: embedding rows + first RMSNorm statistics
+    OP_COUNT = 8
+};
 
 constexpr uint16_t kNoEvent = 0xFFFF;
+constexpr int32_t kMaxSplits = 64;  // attention context splits per (sequence, kv head)
 
 // One task of a worker CTA's queue.  A matvec task computes output rows
 // [a0, a1) of its operator; an attention task covers one (sequence a0, kv
-// head a1) pair over context split a2 of a3.
+// head a1) pair over context split a2 of a3.  On the batched path a
+// projection task covers units [a0, a1) of its operator (see TcGeom) as
+// range number a2, and an embedding task covers items [a0, a1) (item =
+// sequence * H-tiles + H-tile).
 struct Task {
     uint8_t op;
     uint8_t flags;
@@ -30,17 +38,36 @@ struct LayerW {
     const uint16_t *attn_norm, *wq, *wk, *wv, *wo, *mlp_norm, *w_gate, *w_up, *w_down;
 };
 
-// How a matvec operator's weight rows are cut into ring slots: a slot holds
-// `rpp` rows (times 2 for gate/up, which streams matching gate and up rows)
-// of one column piece; a row is cut into `ksplit` pieces of at most `kc`
-// columns when one row does not fit a slot.
+// How a matvec operator's weight rows are cut into ring slots: a row is cut
+// into `ksplit` pieces of `kc` columns (the last may be shorter), and a slot
+// holds piece ks of `rpp` consecutive rows (times 2 for gate/up, which
+// streams matching gate and up rows).
 struct MvGeom {
     int32_t K;        // input length (columns)
     int32_t rows;     // output rows of the operator
     int32_t rpp;      // rows per slot
     int32_t ksplit;   // column pieces per row
-    int32_t kc;       // columns per piece (multiple of 8), last piece may be shorter
+    int32_t kc;       // columns per piece (2048, or K when K is shorter)
     int32_t row_mult; // 2 for gate/up, else 1
+};
+
+// Batched path: an operator's weight [rows x K] is cut into units of
+// kTcTileM rows x kTcTileK columns (one tcgen05 A tile); unit u is row tile
+// u / kchunks, column chunk u % kchunks.  Each worker CTA owns one
+// contiguous range of units (the ranges are balanced to one unit), so a row
+// tile can be shared by several CTAs, whose fp32 partial sums the last one
+// to finish adds up in range order.  The q, k and v matrices are tiled
+// separately: row tiles [0, tiles_q) are q, [tiles_q, tiles_q + tiles_k) k,
+// the rest v.
+constexpr int32_t kTcTileM = 128;
+constexpr int32_t kTcTileK = 64;
+constexpr int32_t kTcMaxBatch = 64;  // MMA N = 2 * npad <= 128; TMEM holds 2 buffers x 2 matrices
+
+struct TcGeom {
+    int32_t K, rows;
+    int32_t tiles, kchunks, units;
+    int32_t tiles_q, tiles_k;  // QKV only
+    int32_t ctr_off;           // first row-tile counter of this operator
 };
 
 // Device error-word sites.
@@ -55,24 +82,29 @@ enum ErrSite : int32_t {
     SITE_POSITION = 7,
     SITE_PAGE = 8,
     SITE_ABORTED = 9,
+    SITE_ACC_WAIT = 10,
 };
 
 // Layout of the plan's control words (uint32 each, zeroed at plan creation).
 //   [0, n_events)                           event counters
 //   [n_events, n_events + batch*n_kv_heads) attention split-done counters
-//   then: exit counter, abort flag, error status, error site, error cta, error detail
+//   then n_tiles row-tile counters (batched path), then: exit counter, abort
+//   flag, error status, error site, error cta, error detail
 struct CtlLayout {
     int32_t n_events;
     int32_t n_done;
+    int32_t tile_idx, n_tiles;
     int32_t exit_idx, abort_idx, err_idx;
     int32_t total;
 };
 
-inline CtlLayout ctl_layout(int32_t n_events, int32_t n_done) {
+inline CtlLayout ctl_layout(int32_t n_events, int32_t n_done, int32_t n_tiles) {
     CtlLayout c;
     c.n_events = n_events;
     c.n_done = n_done;
-    c.exit_idx = n_events + n_done;
+    c.tile_idx = n_events + n_done;
+    c.n_tiles = n_tiles;
+    c.exit_idx = c.tile_idx + n_tiles;
     c.abort_idx = c.exit_idx + 1;
     c.err_idx = c.abort_idx + 1;
     c.total = c.err_idx + 4;

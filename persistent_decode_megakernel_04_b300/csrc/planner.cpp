@@ -30,28 +30,20 @@ namespace mk {
 
 namespace {
 
-int32_t round_up(int32_t a, int32_t b) { return (a + b - 1) / b * b; }
+// A row is cut into pieces of kMvPiece columns (one 16-byte chunk per compute
+// thread), so piece ks of every row meets the same register-resident input
+// chunk in each thread.  A slot holds rpp rows (of each matrix, for gate/up)
+// of one piece; at most 8 accumulators per thread.
+constexpr int32_t kMvPiece = 2048;
 
 MvGeom make_geom(int32_t K, int32_t rows, int32_t row_mult, int32_t slot_bytes) {
     MvGeom g{};
     g.K = K;
     g.rows = rows;
     g.row_mult = row_mult;
-    const int32_t piece_max = slot_bytes / row_mult;
-    const int32_t max_rows = 8 / row_mult;  // accumulators per thread stay <= 8
-    if (K * 2 <= piece_max) {
-        g.ksplit = 1;
-        g.kc = K;
-        g.rpp = std::min(max_rows, piece_max / (K * 2));
-    } else {
-        g.ksplit = (K * 2 + piece_max - 1) / piece_max;
-        for (;;) {
-            g.kc = round_up((K + g.ksplit - 1) / g.ksplit, 8);
-            if (g.kc * 2 <= piece_max) break;
-            ++g.ksplit;
-        }
-        g.rpp = 1;
-    }
+    g.kc = std::min(K, kMvPiece);
+    g.ksplit = (K + g.kc - 1) / g.kc;
+    g.rpp = std::min(8 / row_mult, slot_bytes / (row_mult * g.kc * 2));
     return g;
 }
 
@@ -65,10 +57,12 @@ mk_status check_cfg(const mk_model_cfg &c) {
     if (!(c.rms_eps >= 0.0f) || !(c.rope_theta > 0.0f)) return MK_ERR_INVALID;
     // 16-byte copies need every row length to be a multiple of 8 bf16
     if (c.hidden % 8 || c.ffn_dim % 8 || c.head_dim % 64) return MK_ERR_UNSUPPORTED;
-    if (c.n_layers * 5 >= 0xFFFF) return MK_ERR_UNSUPPORTED;
+    if (c.n_layers * 5 + 1 >= 0xFFFF) return MK_ERR_UNSUPPORTED;
     const int32_t group = c.n_q_heads / c.n_kv_heads;
     if (group > 8 || c.head_dim > 128) return MK_ERR_UNSUPPORTED;
-    if (c.batch != 1) return MK_ERR_UNSUPPORTED;  // batched (tensor-core) tiles: not in this build yet
+    // a matvec input is held in registers: at most 16 row pieces of 2048 columns
+    if (std::max({c.hidden, c.ffn_dim, c.n_q_heads * c.head_dim}) > 16 * kMvPiece) return MK_ERR_UNSUPPORTED;
+    if (c.batch > kTcMaxBatch) return MK_ERR_UNSUPPORTED;  // one tcgen05 N tile holds the whole batch
     return MK_OK;
 }
 
@@ -78,40 +72,86 @@ mk_plan_options resolve_options(const mk_model_cfg &cfg, const mk_plan_options *
     if (opt) o = *opt;
     if (o.num_ctas <= 0 || o.num_ctas > num_sms) o.num_ctas = num_sms;
     if (o.slot_bytes <= 0) o.slot_bytes = 32768;
-    if (o.num_slots <= 0) o.num_slots = 6;
+    if (o.num_slots <= 0) o.num_slots = (cfg.batch > 1) ? 0 : 6;  // batched: as many as shared memory holds
     if (o.timeout_ms <= 0) o.timeout_ms = 2000;
     if (o.attn_splits <= 0) {
         int32_t pairs = cfg.batch * cfg.n_kv_heads;
         o.attn_splits = std::max(1, o.num_ctas / std::max(1, pairs));
     }
+    if (o.attn_splits > kMaxSplits) o.attn_splits = kMaxSplits;
     if (o.l2_prefetch_kb < 0) o.l2_prefetch_kb = 0;
     return o;
 }
+
+namespace {
+
+TcGeom make_tc_geom(int32_t K, int32_t rows, int32_t ctr_off) {
+    TcGeom t{};
+    t.K = K;
+    t.rows = rows;
+    t.tiles = (rows + kTcTileM - 1) / kTcTileM;
+    t.kchunks = (K + kTcTileK - 1) / kTcTileK;
+    t.units = t.tiles * t.kchunks;
+    t.ctr_off = ctr_off;
+    return t;
+}
+
+}  // namespace
 
 mk_status build_plan(const mk_model_cfg &cfg, const mk_plan_options &opt, PlanTables *out) {
     mk_status st = check_cfg(cfg);
     if (st != MK_OK) return st;
     const int32_t N = opt.num_ctas;
-    if (N <= 0 || opt.slot_bytes < 4096 || opt.slot_bytes % 1024 || opt.num_slots < 2 || opt.attn_splits <= 0)
+    const bool tc = cfg.batch > 1;
+    if (N <= 0 || opt.slot_bytes < 4096 || opt.slot_bytes % 1024 || opt.attn_splits <= 0 ||
+        opt.attn_splits > kMaxSplits || (tc ? (opt.num_slots == 1 || opt.num_slots < 0) : opt.num_slots < 2))
         return MK_ERR_INVALID;
     const int32_t H = cfg.hidden, d = cfg.head_dim, nq = cfg.n_q_heads, nkv = cfg.n_kv_heads;
     const int32_t I = cfg.ffn_dim, V = cfg.vocab, L = cfg.n_layers, B = cfg.batch, S = opt.attn_splits;
 
     PlanGeom &g = out->g;
     g = PlanGeom{};
+    g.tc = tc;
     g.num_ctas = N;
     g.attn_splits = S;
-    g.slot_bytes = opt.slot_bytes;
+    g.slot_bytes = tc ? kTcTileM * kTcTileK * 2 : opt.slot_bytes;
     g.num_slots = opt.num_slots;
-    g.tps = std::min(128, opt.slot_bytes / (2 * d * 2));
-    g.n_events = 5 * L;
+    g.tps = std::min(128, g.slot_bytes / (2 * d * 2));
+    g.n_events = 5 * L + (tc ? 1 : 0);
     g.l2_prefetch_bytes = opt.l2_prefetch_kb * 1024;
-    g.mv[OP_QKV] = make_geom(H, (nq + 2 * nkv) * d, 1, opt.slot_bytes);
-    g.mv[OP_O] = make_geom(nq * d, H, 1, opt.slot_bytes);
-    g.mv[OP_GU] = make_geom(H, I, 2, opt.slot_bytes);
-    g.mv[OP_DOWN] = make_geom(I, H, 1, opt.slot_bytes);
-    g.mv[OP_LM] = make_geom(H, V, 1, opt.slot_bytes);
     if (g.tps < 1) return MK_ERR_INVALID;
+    if (!tc) {
+        g.mv[OP_QKV] = make_geom(H, (nq + 2 * nkv) * d, 1, opt.slot_bytes);
+        g.mv[OP_O] = make_geom(nq * d, H, 1, opt.slot_bytes);
+        g.mv[OP_GU] = make_geom(H, I, 2, opt.slot_bytes);
+        g.mv[OP_DOWN] = make_geom(I, H, 1, opt.slot_bytes);
+        g.mv[OP_LM] = make_geom(H, V, 1, opt.slot_bytes);
+        for (int op = OP_QKV; op <= OP_LM; ++op)
+            if (op != OP_ATTN && g.mv[op].rpp < 1) return MK_ERR_INVALID;  // slot smaller than one row piece
+    } else {
+        g.npad = (B + 15) / 16 * 16;
+        // activation tiles hold 2 * npad rows: the bf16 high parts, then the bf16 low parts
+        g.aslot_bytes = 2 * g.npad * kTcTileK * 2;
+        g.num_aslots = std::max(2, std::min(8, (48 * 1024) / g.aslot_bytes));
+        g.h_tiles = (H + kTcTileM - 1) / kTcTileM;
+        int32_t ctr = 0;
+        const int32_t tq = (nq * d + kTcTileM - 1) / kTcTileM, tk = (nkv * d + kTcTileM - 1) / kTcTileM;
+        g.tcg[OP_QKV] = make_tc_geom(H, (nq + 2 * nkv) * d, ctr);
+        g.tcg[OP_QKV].tiles = tq + 2 * tk;  // q, k and v tiled separately
+        g.tcg[OP_QKV].units = g.tcg[OP_QKV].tiles * g.tcg[OP_QKV].kchunks;
+        g.tcg[OP_QKV].tiles_q = tq;
+        g.tcg[OP_QKV].tiles_k = tk;
+        ctr += g.tcg[OP_QKV].tiles;
+        g.tcg[OP_O] = make_tc_geom(nq * d, H, ctr);
+        ctr += g.tcg[OP_O].tiles;
+        g.tcg[OP_GU] = make_tc_geom(H, I, ctr);
+        ctr += g.tcg[OP_GU].tiles;
+        g.tcg[OP_DOWN] = make_tc_geom(I, H, ctr);
+        ctr += g.tcg[OP_DOWN].tiles;
+        g.tcg[OP_LM] = make_tc_geom(H, V, ctr);
+        ctr += g.tcg[OP_LM].tiles;
+        g.n_tile_ctrs = ctr;
+    }
 
     // CTA permutation (identity unless a planner seed is given)
     std::vector<int32_t> perm(N);
@@ -121,12 +161,17 @@ mk_status build_plan(const mk_model_cfg &cfg, const mk_plan_options &opt, PlanTa
         std::shuffle(perm.begin(), perm.end(), rng);
     }
 
+    // Work items of a projection: output rows (batch 1) or units (batched).
+    auto items = [&](int32_t op) -> int32_t { return tc ? g.tcg[op].units : g.mv[op].rows; };
+
     std::vector<std::vector<Task>> q(N);
-    auto emit_matvec = [&](int32_t op, int32_t layer, int32_t rows, uint16_t wait_ev, uint32_t wait_cnt,
+    // Cuts `total` items into one contiguous range per CTA (balanced to one
+    // item); range c goes to CTA perm[c].  Returns the number of tasks.
+    auto emit_ranges = [&](int32_t op, int32_t layer, int32_t total, uint16_t wait_ev, uint32_t wait_cnt,
                            uint16_t sig_ev) -> uint32_t {
         uint32_t n = 0;
         for (int32_t c = 0; c < N; ++c) {
-            int32_t r0 = (int32_t)((int64_t)c * rows / N), r1 = (int32_t)((int64_t)(c + 1) * rows / N);
+            int32_t r0 = (int32_t)((int64_t)c * total / N), r1 = (int32_t)((int64_t)(c + 1) * total / N);
             if (r1 <= r0) continue;
             Task t{};
             t.op = (uint8_t)op;
@@ -136,19 +181,26 @@ mk_status build_plan(const mk_model_cfg &cfg, const mk_plan_options &opt, PlanTa
             t.signal_ev = sig_ev;
             t.a0 = r0;
             t.a1 = r1;
+            t.a2 = c;
             q[perm[c]].push_back(t);
             ++n;
         }
         return n;
     };
-    auto count_ranges = [&](int32_t rows) { return (uint32_t)std::min<int64_t>(rows, N); };
+    auto count_ranges = [&](int32_t total) { return (uint32_t)std::min<int64_t>(total, N); };
 
-    const uint32_t n_qkv = count_ranges(g.mv[OP_QKV].rows), n_o = count_ranges(H), n_gu = count_ranges(I),
-                   n_down = count_ranges(H);
     uint16_t x_ready_ev = kNoEvent;
     uint32_t x_ready_cnt = 0;
+    if (tc) {
+        // embedding rows and the first RMSNorm statistics, one item per (sequence, H tile)
+        const uint16_t ev = (uint16_t)(5 * L);
+        x_ready_cnt = emit_ranges(OP_EMBED, 0, B * g.h_tiles, kNoEvent, 0, ev);
+        x_ready_ev = ev;
+    }
+    const uint32_t n_qkv = count_ranges(items(OP_QKV)), n_o = count_ranges(items(OP_O)),
+                   n_gu = count_ranges(items(OP_GU)), n_down = count_ranges(items(OP_DOWN));
     for (int32_t l = 0; l < L; ++l) {
-        uint32_t k = emit_matvec(OP_QKV, l, g.mv[OP_QKV].rows, x_ready_ev, x_ready_cnt, (uint16_t)ev_id(l, OP_QKV));
+        uint32_t k = emit_ranges(OP_QKV, l, items(OP_QKV), x_ready_ev, x_ready_cnt, (uint16_t)ev_id(l, OP_QKV));
         if (k != n_qkv) return MK_ERR_INVALID;
         // attention: one task per (sequence, kv head, split), round-robin over CTAs
         int32_t i = 0;
@@ -167,13 +219,13 @@ mk_status build_plan(const mk_model_cfg &cfg, const mk_plan_options &opt, PlanTa
                     t.a3 = S;
                     q[perm[i % N]].push_back(t);
                 }
-        emit_matvec(OP_O, l, H, (uint16_t)ev_id(l, OP_ATTN), (uint32_t)(B * nkv), (uint16_t)ev_id(l, OP_O));
-        emit_matvec(OP_GU, l, I, (uint16_t)ev_id(l, OP_O), n_o, (uint16_t)ev_id(l, OP_GU));
-        emit_matvec(OP_DOWN, l, H, (uint16_t)ev_id(l, OP_GU), n_gu, (uint16_t)ev_id(l, OP_DOWN));
+        emit_ranges(OP_O, l, items(OP_O), (uint16_t)ev_id(l, OP_ATTN), (uint32_t)(B * nkv), (uint16_t)ev_id(l, OP_O));
+        emit_ranges(OP_GU, l, items(OP_GU), (uint16_t)ev_id(l, OP_O), n_o, (uint16_t)ev_id(l, OP_GU));
+        emit_ranges(OP_DOWN, l, items(OP_DOWN), (uint16_t)ev_id(l, OP_GU), n_gu, (uint16_t)ev_id(l, OP_DOWN));
         x_ready_ev = (uint16_t)ev_id(l, OP_DOWN);
         x_ready_cnt = n_down;
     }
-    emit_matvec(OP_LM, L - 1, V, x_ready_ev, x_ready_cnt, kNoEvent);
+    emit_ranges(OP_LM, L - 1, items(OP_LM), x_ready_ev, x_ready_cnt, kNoEvent);
 
     if (opt.test_unreachable_event > 0) {
         const int32_t ev = opt.test_unreachable_event - 1;

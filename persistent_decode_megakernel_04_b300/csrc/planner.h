@@ -17,6 +17,14 @@ struct PlanGeom {
     int32_t n_events = 0;
     int32_t l2_prefetch_bytes = 0;
     MvGeom mv[OP_COUNT] = {};
+    // batched (tensor-core) path
+    bool tc = false;
+    int32_t npad = 0;         // batch rounded up to the MMA N granule (16)
+    int32_t aslot_bytes = 0;  // activation ring slot: npad rows x 64 bf16
+    int32_t num_aslots = 0;
+    int32_t h_tiles = 0;      // 128-row tiles of the hidden size
+    int32_t n_tile_ctrs = 0;  // row-tile counters of all projections
+    TcGeom tcg[OP_COUNT] = {};
 };
 
 struct PlanTables {

@@ -131,3 +131,69 @@ def run_from_cache(plan: mk.Plan, kv: mk.KVCache, model: oracle.Model, caches: d
             stats.append(compare_logits(got[b], ref, f"row {b} step {i} (pos {pos})"))
             tok_h[b] = int(np.argmax(ref))
     return stats
+
+
+def run_teacher_forced_batch(plan: mk.Plan, kv: mk.KVCache, model: oracle.Model, prompts: np.ndarray, steps: int,
+                             max_seq: int, rows=None, ablation_every: int = 0):
+    """Batched form of run_teacher_forced: prompts [B][T] are prefilled
+    together; every decode step feeds each checked row the ORACLE's greedy
+    token (unchecked rows follow the GPU's own greedy token).  Compares the
+    checked rows' logits at every step."""
+    import torch
+
+    dev = torch.device("cuda")
+    B, T = prompts.shape
+    V = model.cfg.vocab
+    rows = list(range(B)) if rows is None else list(rows)
+    caches = {b: model.new_cache(max_seq) for b in rows}
+    refs = {b: model.prefill(caches[b][0], caches[b][1], prompts[b]) for b in rows}
+    logits = torch.empty((B, V), dtype=torch.float32, device=dev)
+    plan.prefill(torch.tensor(prompts, dtype=torch.int32, device=dev), kv, logits)
+    plan.check()
+    got = logits.cpu().numpy()
+    stats = [compare_logits(got[b], refs[b], f"prefill row {b}") for b in rows]
+    tok = np.argmax(got, axis=1).astype(np.int32)
+    for i in range(steps):
+        pos = T + i
+        for b in rows:
+            tok[b] = int(np.argmax(refs[b]))
+            refs[b] = model.decode_step(caches[b][0], caches[b][1], int(tok[b]), pos)
+        tok_d = torch.tensor(tok, device=dev)
+        pos_d = torch.full((B,), pos, dtype=torch.int32, device=dev)
+        if ablation_every and i % ablation_every == 0:
+            plan.decode_step_ablation(tok_d, pos_d, kv, logits)
+        else:
+            plan.decode_step(tok_d, pos_d, kv, logits)
+        plan.check()
+        got = logits.cpu().numpy()
+        stats += [compare_logits(got[b], refs[b], f"row {b} decode step {i} (pos {pos})") for b in rows]
+        tok = np.argmax(got, axis=1).astype(np.int32)
+    return stats
+
+
+def run_from_cache_ragged(plan: mk.Plan, kv: mk.KVCache, model: oracle.Model, caches: dict, ctxs, steps: int,
+                          first_tokens, batch: int):
+    """Decode steps from a seeded cache where row b starts at its own
+    position ctxs[b] (ragged contexts).  Checked rows (the keys of `caches`)
+    are teacher-forced with the oracle's greedy token."""
+    import torch
+
+    dev = torch.device("cuda")
+    V = model.cfg.vocab
+    tok_h = np.array(first_tokens, dtype=np.int32)
+    pos_h = np.array(ctxs, dtype=np.int32)
+    logits = torch.empty((batch, V), dtype=torch.float32, device=dev)
+    stats = []
+    for i in range(steps):
+        refs = {b: model.decode_step(caches[b][0], caches[b][1], int(tok_h[b]), int(pos_h[b])) for b in caches}
+        plan.decode_step(torch.tensor(tok_h, device=dev), torch.tensor(pos_h, device=dev), kv, logits)
+        plan.check()
+        got = logits.cpu().numpy()
+        for b, ref in refs.items():
+            stats.append(compare_logits(got[b], ref, f"row {b} step {i} (pos {pos_h[b]})"))
+            tok_h[b] = int(np.argmax(ref))
+        for b in range(batch):
+            if b not in caches:
+                tok_h[b] = int(np.argmax(got[b]))
+        pos_h += 1
+    return stats

@@ -1,0 +1,94 @@
+"""GPU parity of the batched decode path (tcgen05 tensor-core projections,
+fused epilogues, stream-K row tiles) against the fp64 oracle, through the C
+ABI.  Same tolerances as the batch-1 path (tests/harness.py)."""
+import numpy as np
+import pytest
+
+import persistent_decode_megakernel_04_b300 as mk
+import synth
+from synth import WORKLOADS
+from tests import harness
+
+pytestmark = pytest.mark.gpu
+
+TINY = WORKLOADS["tiny"].model
+
+
+def prompts(B, T, seed=0, vocab=TINY.vocab):
+    return np.stack([synth.tokens(T, seed, 100 + b, vocab) for b in range(B)])
+
+
+@pytest.mark.parametrize("B", [2, 16, 24, 64])
+def test_tiny_batched_prompt_and_decode(cuda_device, B):
+    # B=24 pads the MMA N to 32 (rows 24..31 of the activation tiles read as zero)
+    max_seq = 128
+    plan, kv = harness.gpu_plan(TINY, max_seq, batch=B)
+    model = harness.oracle_model(TINY)
+    rows = sorted({0, 1, B // 2, B - 1})
+    harness.run_teacher_forced_batch(plan, kv, model, prompts(B, 20), 6, max_seq, rows=rows)
+
+
+def test_tiny_batched_random_gains_and_ablation(cuda_device):
+    m = synth.with_random_gains(TINY)
+    max_seq = 128
+    plan, kv = harness.gpu_plan(m, max_seq, batch=8)
+    model = harness.oracle_model(m)
+    harness.run_teacher_forced_batch(plan, kv, model, prompts(8, 12, seed=3), 4, max_seq, rows=[0, 3, 7],
+                                     ablation_every=2)
+
+
+@pytest.mark.parametrize("opts", [dict(num_ctas=7, attn_splits=3, planner_seed=5),
+                                  dict(num_ctas=148, attn_splits=1, num_slots=3, planner_seed=9),
+                                  dict(num_ctas=1)], ids=["7ctas", "3slots", "1cta"])
+def test_tiny_batched_schedules(cuda_device, opts):
+    # row tiles shared by several ranges (fixup), a permuted CTA assignment,
+    # a shallow weight ring and a single worker CTA
+    max_seq = 128
+    plan, kv = harness.gpu_plan(TINY, max_seq, batch=4, opts=mk.mk_plan_options(**opts))
+    model = harness.oracle_model(TINY)
+    harness.run_teacher_forced_batch(plan, kv, model, prompts(4, 70, seed=2), 3, max_seq, rows=[0, 3])
+
+
+def test_tiny_batched_ragged_positions(cuda_device):
+    B, max_seq = 6, 256
+    plan, kv = harness.gpu_plan(TINY, max_seq, batch=B)
+    model = harness.oracle_model(TINY)
+    ctx = 150
+    caches = harness.fill_synthetic_cache(kv, model, TINY, ctx, B, max_seq, rows=(0, 2, 5))
+    ctxs = [ctx - 37 * b % 140 for b in range(B)]  # every row at its own position
+    harness.run_from_cache_ragged(plan, kv, model, caches, ctxs, 3, synth.tokens(B, 0, 9, TINY.vocab), B)
+
+
+def test_batched_rows_equal_single_sequence_runs(cuda_device):
+    """Row b of a batched step equals the same sequence run alone (batch 1
+    path) to within the parity tolerance."""
+    import torch
+
+    B, T, max_seq = 4, 16, 64
+    P = prompts(B, T, seed=7)
+    plan, kv = harness.gpu_plan(TINY, max_seq, batch=B)
+    logits = torch.empty((B, TINY.vocab), dtype=torch.float32, device=cuda_device)
+    plan.prefill(torch.tensor(P, dtype=torch.int32, device=cuda_device), kv, logits)
+    plan.check()
+    got = logits.cpu().numpy()
+    for b in range(B):
+        p1, kv1 = harness.gpu_plan(TINY, max_seq, batch=1)
+        l1 = torch.empty((1, TINY.vocab), dtype=torch.float32, device=cuda_device)
+        p1.prefill(torch.tensor(P[b:b + 1], dtype=torch.int32, device=cuda_device), kv1, l1)
+        p1.check()
+        harness.compare_logits(got[b], l1.cpu().numpy()[0], f"row {b} vs batch-1 run")
+
+
+@pytest.mark.parametrize("B", [8, 64])
+def test_8b_batched_decode_from_seeded_cache(cuda_device, B):
+    """The 8B-shaped decoder at 4096 cached tokens per sequence (paged,
+    shuffled pages), in the launch configuration the bench times; the oracle
+    checks rows 0 and B-1."""
+    wl = WORKLOADS["8b-batch"]
+    m = wl.model
+    ctx, steps = 4096, 2
+    max_seq = ((ctx + steps + 64) // 64) * 64
+    plan, kv = harness.gpu_plan(m, max_seq, batch=B)
+    model = harness.oracle_model(m)
+    caches = harness.fill_synthetic_cache(kv, model, m, ctx, B, max_seq, rows=(0, B - 1))
+    harness.run_from_cache(plan, kv, model, caches, ctx, steps, synth.tokens(B, wl.seed, 0, m.vocab), batch=B)

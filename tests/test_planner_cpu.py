@@ -52,7 +52,7 @@ def test_attention_tasks_cover_every_head_and_split(name):
     m, tasks, _ = describe(name, 148)
     att = [t for t in tasks if t.op == mk.OP_ATTN]
     S = att[0].a3
-    assert S == max(1, 148 // m.n_kv_heads)
+    assert S == min(64, max(1, 148 // m.n_kv_heads))  # default splits, capped at 64
     seen = {(t.layer, t.a0, t.a1, t.a2) for t in att}
     assert len(seen) == len(att) == m.n_layers * m.n_kv_heads * S
 
@@ -135,3 +135,79 @@ def test_planner_seed_permutes_assignment_but_not_work():
     key = lambda t: (t.layer, t.op, t.a0, t.a1, t.a2)
     assert sorted(map(key, a)) == sorted(map(key, b))
     assert [t.cta for t in sorted(a, key=key)] != [t.cta for t in sorted(b, key=key)]
+
+
+# ------------------------------------------------------------ batched path
+
+def describe_b(name, B, num_ctas, **kw):
+    m = SHAPES[name]
+    cfg = mk.model_cfg(m, B, 1024)
+    opts = mk.mk_plan_options(**kw) if kw else None
+    tasks, n_events = mk.mk_plan_describe(cfg, num_ctas, opts)
+    return m, tasks, n_events
+
+
+def tc_units(m, op):
+    T, K = mk.TC_TILE_M, mk.TC_TILE_K
+    cdiv = lambda a, b: (a + b - 1) // b
+    d = m.head_dim
+    if op == mk.OP_QKV:
+        tiles = cdiv(m.n_q_heads * d, T) + 2 * cdiv(m.n_kv_heads * d, T)
+        return tiles * cdiv(m.hidden, K), cdiv(m.hidden, K)
+    rows, k = {mk.OP_O: (m.hidden, m.n_q_heads * d), mk.OP_GU: (m.ffn_dim, m.hidden),
+               mk.OP_DOWN: (m.hidden, m.ffn_dim), mk.OP_LM: (m.vocab, m.hidden)}[op]
+    return cdiv(rows, T) * cdiv(k, K), cdiv(k, K)
+
+
+@pytest.mark.parametrize("name", list(SHAPES))
+@pytest.mark.parametrize("B,num_ctas", [(2, 148), (64, 148), (16, 37), (8, 1)])
+def test_batched_units_covered_once_and_balanced(name, B, num_ctas):
+    m, tasks, _ = describe_b(name, B, num_ctas)
+    cover = defaultdict(list)
+    for t in tasks:
+        if t.op not in (mk.OP_ATTN,):
+            cover[(t.layer, t.op)].append((t.a0, t.a1, t.a2))
+    for l in range(m.n_layers):
+        for op in (mk.OP_QKV, mk.OP_O, mk.OP_GU, mk.OP_DOWN):
+            U, _ = tc_units(m, op)
+            rs = sorted(cover[(l, op)])
+            assert rs[0][0] == 0 and rs[-1][1] == U
+            assert all(a[1] == b[0] for a, b in zip(rs, rs[1:])), "gap or overlap"
+            sizes = [b - a for a, b, _ in rs]
+            assert max(sizes) - min(sizes) <= 1
+            # range number c owns [c*U/N, (c+1)*U/N)
+            for a0, a1, c in rs:
+                assert (a0, a1) == (c * U // num_ctas, (c + 1) * U // num_ctas)
+    emb = sorted(cover[(0, mk.OP_EMBED)])
+    h_tiles = (m.hidden + mk.TC_TILE_M - 1) // mk.TC_TILE_M
+    assert emb[0][0] == 0 and emb[-1][1] == B * h_tiles
+
+
+@pytest.mark.parametrize("U,N", [(16, 148), (3072, 148), (64128, 148), (7168, 37), (100, 7), (5, 5)])
+def test_stream_k_tile_contributors(U, N):
+    """The device finds the ranges sharing a row tile from closed forms:
+    range_of(u) = ((u+1)N - 1) div U owns unit u, range_start(c) = cU div N.
+    Checked against the ranges themselves."""
+    starts = [c * U // N for c in range(N + 1)]
+    owner = {}
+    for c in range(N):
+        for u in range(starts[c], starts[c + 1]):
+            owner[u] = c
+    for u in range(U):
+        assert ((u + 1) * N - 1) // U == owner[u]
+
+
+@pytest.mark.parametrize("name", ["tiny", "8b"])
+@pytest.mark.parametrize("B,num_ctas,seed", [(8, 148, 0), (64, 148, 3), (4, 5, 1)])
+def test_batched_schedule_completes(name, B, num_ctas, seed):
+    m, tasks, n_events = describe_b(name, B, num_ctas, planner_seed=seed)
+    assert n_events == 5 * m.n_layers + 1
+    ok, order, _ = simulate(m, tasks, n_events)
+    assert ok, "deadlock: some queue never drained"
+    pos = {}
+    for i, t in enumerate(order):
+        pos.setdefault((t.layer, t.op), []).append(i)
+    assert min(pos[(0, mk.OP_QKV)]) > max(pos[(0, mk.OP_EMBED)])
+    for l in range(m.n_layers):
+        assert min(pos[(l, mk.OP_ATTN)]) > max(pos[(l, mk.OP_QKV)])
+        assert min(pos[(l, mk.OP_DOWN)]) > max(pos[(l, mk.OP_GU)])
