@@ -176,6 +176,37 @@ mk_status mk_greedy_next(mk_plan *plan, const float *logits, int32_t *tokens, in
 mk_status mk_plan_trace(mk_plan *plan, void *stream, uint64_t *out, int64_t capacity, int32_t *num_ctas,
                         int32_t *max_tasks);
 
+/* Batch-1 decode step that allocates no device memory.
+ *
+ * The pages have no counterpart to this call. It exists for callers that
+ * cannot call cudaMalloc when they need a decode step: code running while a
+ * memory pool or a CUDA graph owns the device's allocations, a runtime that
+ * reserves all device memory up front, or a serving process that must not
+ * grow its footprint. It needs no plan. Each call builds the task graph on
+ * the host from `cfg` (batch must be 1; other values return
+ * MK_ERR_UNSUPPORTED), then runs the same persistent kernel as
+ * mk_decode_step, with the same arguments and results.
+ *
+ * Scratch: every call uses one fixed 16 MiB device array, compiled into this
+ * library. Every GPU that loads the library holds those 16 MiB until the
+ * process exits. A shape whose task tables, activations, attention partials
+ * and RoPE table (max_seq x head_dim/2 x 8 bytes) need more returns MK_ERR_OOM
+ * before anything is launched. The array keeps the last call's contents, so
+ * each call uploads its tables and clears its counters and error word before
+ * the launch. Calls that overlap on the GPU (on two streams at once) share the
+ * array and race: issue them one at a time.
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (cudaGetSymbolAddress). Make that first call before any stream
+ * capture. The call calls no cudaMalloc or cudaFree.
+ *
+ * The call is synchronous: it synchronises `stream` and returns the step's
+ * device-detected error (MK_ERR_BOUNDS, MK_ERR_TIMEOUT), if any, as its
+ * status. weights, tokens, positions, kv and logits are as for
+ * mk_plan_create and mk_decode_step. */
+mk_status mk_decode_step_noalloc(const mk_model_cfg *cfg, const mk_weight_ptrs *w, const int32_t *tokens,
+                                 const int32_t *positions, const mk_kv_cache *kv, float *logits, void *stream);
+
 /* Synchronises `stream`, reads and clears the plan's device error word. */
 mk_status mk_plan_last_error(mk_plan *plan, void *stream, mk_device_error *info);
 

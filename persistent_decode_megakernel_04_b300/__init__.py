@@ -57,7 +57,7 @@ class mk_task_info(ctypes.Structure):
 _lib = None
 EXPORTS = ("mk_plan_create", "mk_plan_create_ex", "mk_decode_step", "mk_decode_step_ablation",
            "mk_decode_step_host", "mk_prefill", "mk_greedy_next", "mk_plan_last_error", "mk_status_string",
-           "mk_error_site_string", "mk_plan_destroy", "mk_plan_describe", "mk_plan_trace")
+           "mk_error_site_string", "mk_plan_destroy", "mk_plan_describe", "mk_plan_trace", "mk_decode_step_noalloc")
 
 
 def lib():
@@ -85,6 +85,7 @@ def lib():
         L.mk_plan_describe.argtypes = [P(mk_model_cfg), P(mk_plan_options), _i32, P(mk_task_info), _i32,
                                        P(_i32), P(_i32)]
         L.mk_plan_trace.argtypes = [_vp, _vp, _vp, ctypes.c_int64, P(_i32), P(_i32)]
+        L.mk_decode_step_noalloc.argtypes = [P(mk_model_cfg), P(mk_weight_ptrs), _vp, _vp, P(mk_kv_cache), _vp, _vp]
         for n in EXPORTS:
             if n not in ("mk_plan_destroy", "mk_status_string", "mk_error_site_string"):
                 getattr(L, n).restype = ctypes.c_int
