@@ -169,7 +169,12 @@ mk_status mk_greedy_next(mk_plan *plan, const float *logits, int32_t *tokens, in
  *   k=1 compute warps started it, k=2 they finished it,
  *   k=3 total time the compute warps waited for ring slots to fill,
  *   k=4 producer issued the task's first copy,
- *   k=5 total time the producer waited for free ring slots.
+ *   k=5 total time the producer waited for free ring slots,
+ *   k=6 (batched projections) total time the MMA issuer waited for
+ *       activation tiles, k=7 ... for a free TMEM accumulator.
+ * On the batched path k=3 of a projection task is the MMA issuer's wait for
+ * weight tiles.  For attention tasks k=6 is the time spent in slot waits and
+ * scores, k=7 the time in value sums (the rest is softmax and per-task work).
  * Zeros mark tasks not run.  Synchronises `stream`.  Host buffer of
  * `capacity` uint64 values; MK_ERR_INVALID if tracing is off or the buffer is
  * too small (*max_tasks is still set). */

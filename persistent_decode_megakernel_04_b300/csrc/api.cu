@@ -45,6 +45,50 @@ struct mk_plan {
     KParams base{};
 };
 
+namespace mk {
+
+// cuTensorMapEncodeTiled from the driver, looked up once (no libcuda link).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        else
+            cudaGetLastError();
+    }
+    return fn;
+}
+
+// Row-major bf16 [outer][inner] matrix read in boxes of 64 columns x
+// box_outer rows, 128-byte swizzled (the tcgen05 K-major operand layout).
+// Rows and columns past the end read as zero.
+bool encode_bf16_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {inner * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kTcTileK, box_outer};
+    const cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// K and V pools as [L * num_pages * nkv * page_size][d] bf16 rows, read in
+// boxes of 64 columns x ts tokens.
+bool encode_kv_maps(KParams &k, const mk_model_cfg &c, const mk_kv_cache &kv, int32_t ts) {
+    const uint64_t rows = (uint64_t)c.n_layers * kv.num_pages * c.n_kv_heads * c.page_size;
+    if (rows >= (1ull << 31)) return false;
+    return encode_bf16_2d(reinterpret_cast<CUtensorMap *>(k.kv_maps[0]), kv.k_pool, c.head_dim, rows, ts) &&
+           encode_bf16_2d(reinterpret_cast<CUtensorMap *>(k.kv_maps[1]), kv.v_pool, c.head_dim, rows, ts);
+}
+
+}  // namespace mk
+
 namespace {
 
 template <typename T>
@@ -78,38 +122,9 @@ mk_status check_kv(const mk_plan *p, const mk_kv_cache *kv) {
     if (!kv || !aligned16(kv->k_pool) || !aligned16(kv->v_pool) || !aligned16(kv->page_table)) return MK_ERR_INVALID;
     if (kv->num_pages <= 0 || kv->max_pages_per_seq <= 0) return MK_ERR_INVALID;
     if ((int64_t)kv->max_pages_per_seq * p->cfg.page_size < p->cfg.max_seq) return MK_ERR_INVALID;
+    KParams probe{};
+    if (!encode_kv_maps(probe, p->cfg, *kv, p->tables.g.tps)) return MK_ERR_INVALID;  // pools too large for a map
     return MK_OK;
-}
-
-// cuTensorMapEncodeTiled from the driver, looked up once (no libcuda link).
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-        else
-            cudaGetLastError();
-    }
-    return fn;
-}
-
-// Row-major bf16 [outer][inner] matrix read in boxes of 64 columns x
-// box_outer rows, 128-byte swizzled (the tcgen05 K-major operand layout).
-// Rows and columns past the end read as zero.
-bool encode_bf16_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-    if (!enc) return false;
-    const cuuint64_t dims[2] = {inner, outer};
-    const cuuint64_t strides[1] = {inner * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kTcTileK, box_outer};
-    const cuuint32_t es[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 mk_status cuda_status(cudaError_t e) {
@@ -128,6 +143,7 @@ void free_plan(mk_plan *p) {
 KParams step_params(const mk_plan *p, const int32_t *tokens, int32_t tok_stride, const int32_t *positions,
                     int32_t pos_stride, const mk_kv_cache *kv, float *logits) {
     KParams k = p->base;
+    encode_kv_maps(k, p->cfg, *kv, p->tables.g.tps);  // checked by check_kv
     k.k_pool = static_cast<uint16_t *>(kv->k_pool);
     k.v_pool = static_cast<uint16_t *>(kv->v_pool);
     k.page_table = kv->page_table;
@@ -403,7 +419,7 @@ mk_status mk_plan_create_ex(const mk_model_cfg *cfg, const mk_weight_ptrs *w, co
     for (int i = 0; i < OP_COUNT; ++i) k.mv[i] = g.mv[i];
     k.slot_bytes = g.slot_bytes;
     k.num_slots = g.num_slots;
-    k.tps = g.tps;
+    k.attn_ts = g.tps;
     k.attn_splits = g.attn_splits;
     k.l2_prefetch_bytes = g.l2_prefetch_bytes;
     k.only_op = -1;

@@ -58,8 +58,11 @@ struct SmemCtl {
     float att_inv_l[kMaxGroup];
     float merge_w[kMaxSplits][kMaxGroup];  // split weights exp(m_s - max_s m_s) of the merge
     float resid[kMaxResid];                // residual rows of an O / down task, read at task start
-    alignas(16) float q_s[kMaxGroup][kMaxHeadDim];
-    alignas(16) float s_s[kMaxGroup][kMaxTps];
+    alignas(16) float q_s[kMaxGroup][kMaxHeadDim];        // RoPE'd, scaled queries (fp32)
+    alignas(16) float s_s[kMaxGroup][kAttnBlock];         // scores of one 64-token block
+    alignas(16) uint16_t q_hl[2 * kMaxGroup][kQhlStride];  // queries as bf16 high parts, then low parts
+    alignas(16) uint16_t p_hl[2 * kMaxGroup][kPhlStride];  // softmax weights, bf16 high then low parts
+    float att_pnew[kMaxGroup];                             // weight of the new token
     alignas(16) uint16_t knew[kMaxHeadDim];
     alignas(16) uint16_t vnew[kMaxHeadDim];
     // batched (tensor-core) path
@@ -193,20 +196,28 @@ __device__ void record_error(const Ctx &c, int32_t status, int32_t site, int32_t
 
 // Bounded wait on an mbarrier phase.  Returns false on abort or timeout; a
 // failure always leaves the CTA marked aborted.
+// The abort flags and the time budget are checked every kAbortCheckNs only:
+// the grid-wide flag is a global-memory load whose latency would otherwise
+// sit between a phase completing and the waiter noticing it.
+constexpr uint64_t kAbortCheckNs = 20000;
+
 __device__ bool wait_mbar(const Ctx &c, uint64_t *bar, uint32_t parity, int32_t site) {
     if (mbar_try_wait(bar, parity)) return true;
-    uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 15u) == 0) {
+    const uint64_t t0 = globaltimer_ns();
+    uint64_t next = t0 + kAbortCheckNs;
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 1000u)) return true;
+        const uint64_t now = globaltimer_ns();
+        if (now >= next) {
             if (local_abort(c) || global_abort(*c.p)) {
                 set_local_abort(c);
                 return false;
             }
-            if (globaltimer_ns() - t0 > c.p->timeout_ns) {
+            if (now - t0 > c.p->timeout_ns) {
                 record_error(c, 4 /*MK_ERR_TIMEOUT*/, site, (int32_t)parity);
                 return false;
             }
+            next = now + kAbortCheckNs;
         }
     }
 }
@@ -226,10 +237,10 @@ __device__ __forceinline__ int32_t mv_group_rows(const KParams &p, int op, int32
     return n;
 }
 
-// matrix and local row of operator row `row`
-__device__ __forceinline__ const uint16_t *mv_matrix(const KParams &p, int op, int layer, int32_t row,
+// matrix and local row of operator row `row` (w: the layer's pointers, held
+// in registers by the caller)
+__device__ __forceinline__ const uint16_t *mv_matrix(const KParams &p, int op, const LayerW &w, int32_t row,
                                                      int32_t *local) {
-    const LayerW &w = p.layers[layer];
     *local = row;
     switch (op) {
         case OP_QKV: {
@@ -250,19 +261,20 @@ __device__ __forceinline__ const uint16_t *mv_matrix(const KParams &p, int op, i
 }
 
 struct AttnRange {
-    int32_t pos, lo, cend;  // cached tokens [lo, cend); new token at pos
-    bool has_new;
+    int32_t pos;       // position of the new token
+    int32_t blo, bhi;  // 64-token blocks [blo, bhi) of the cached context [0, pos)
+    bool has_new;      // this split also attends to the new token
 };
 
-// Split s of S covers context positions [s*C/S, (s+1)*C/S) of C = pos + 1;
-// the last split always holds the new token.
+// The cached context [0, pos) is cut into aligned 64-token blocks, and split
+// s of S takes blocks [s*nb/S, (s+1)*nb/S); the last split also handles the
+// new token at pos, which is not read from the cache.
 __device__ __forceinline__ AttnRange attn_range(const KParams &p, const Task &t) {
     AttnRange r;
     r.pos = p.positions[(int64_t)t.a0 * p.pos_stride];
-    const int64_t C = (int64_t)r.pos + 1;
-    r.lo = (int32_t)((int64_t)t.a2 * C / t.a3);
-    const int32_t hi = (int32_t)((int64_t)(t.a2 + 1) * C / t.a3);
-    r.cend = min(hi, r.pos);
+    const int64_t nb = (r.pos + kAttnBlock - 1) / kAttnBlock;
+    r.blo = (int32_t)((int64_t)t.a2 * nb / t.a3);
+    r.bhi = (int32_t)((int64_t)(t.a2 + 1) * nb / t.a3);
     r.has_new = (t.a2 == t.a3 - 1);
     return r;
 }
@@ -277,10 +289,12 @@ struct Producer {
     uint32_t issued = 0;
     uint64_t pol;
     uint64_t *tr = nullptr;  // trace entry of the current task
+    uint32_t ns = 0;         // ring slots (kept in a register)
+    uint32_t slot_bytes = 0;
 
     __device__ bool acquire_slot(const Ctx &c, uint32_t *slot) {
-        const uint32_t s = issued % (uint32_t)c.p->num_slots;
-        const uint32_t round = issued / (uint32_t)c.p->num_slots;
+        const uint32_t s = issued % ns;
+        const uint32_t round = issued / ns;
         const uint64_t t0 = tr ? globaltimer_ns() : 0;
         if (!wait_mbar(c, &c.sc->empty[s], (round & 1u) ^ 1u, SITE_EMPTY_WAIT)) return false;
         if (tr) {
@@ -295,21 +309,22 @@ struct Producer {
     __device__ bool run_matvec(const Ctx &c, const Task &t) {
         const KParams &p = *c.p;
         const int op = t.op;
-        const MvGeom &g = p.mv[op];
+        const MvGeom g = p.mv[op];              // register copies: the copy loop's
+        const LayerW lw = p.layers[t.layer];    // inline asm must not force reloads
         for (int32_t row = t.a0; row < t.a1;) {
             const int32_t n = mv_group_rows(p, op, row, t.a1);
             int32_t lr;
-            const uint16_t *W = mv_matrix(p, op, t.layer, row, &lr);
+            const uint16_t *W = mv_matrix(p, op, lw, row, &lr);
             for (int32_t ks = 0; ks < g.ksplit; ++ks) {
                 uint32_t s;
                 if (!acquire_slot(c, &s)) return false;
                 const int32_t k0 = ks * g.kc;
                 const int32_t pw = min(g.kc, g.K - k0);
                 const uint32_t bytes = (uint32_t)(g.row_mult * n * pw * 2);
-                uint8_t *dst = c.ring + (size_t)s * p.slot_bytes;
+                uint8_t *dst = c.ring + (size_t)s * slot_bytes;
                 mbar_arrive_expect_tx(&c.sc->full[s], bytes);
                 for (int m = 0; m < g.row_mult; ++m) {
-                    const uint16_t *Wm = (m == 0) ? W : p.layers[t.layer].w_up;
+                    const uint16_t *Wm = (m == 0) ? W : lw.w_up;
                     if (g.ksplit == 1) {
                         bulk_g2s(dst + (size_t)m * n * pw * 2, Wm + (int64_t)lr * g.K, (uint32_t)(n * pw * 2),
                                  &c.sc->full[s], pol);
@@ -326,27 +341,30 @@ struct Producer {
         return true;
     }
 
+    // KV of one 64-token block: TMA tiles of ts tokens x 64 columns (128-byte
+    // swizzle) from the paged pools, K halves then V halves, in 64/ts slots.
     __device__ bool run_attn(const Ctx &c, const Task &t) {
         const KParams &p = *c.p;
         const AttnRange r = attn_range(p, t);
-        const int32_t tps = p.tps;
+        const int ts = p.attn_ts, halves = p.d / 64;
         const int32_t *pt = p.page_table + (int64_t)t.a0 * p.max_pages;
-        for (int32_t t0 = r.lo; t0 < r.cend; t0 += tps) {
-            const int32_t t1 = min(r.cend, t0 + tps);
-            uint32_t s;
-            if (!acquire_slot(c, &s)) return false;
-            uint8_t *dst = c.ring + (size_t)s * p.slot_bytes;
-            mbar_arrive_expect_tx(&c.sc->full[s], (uint32_t)(2 * (t1 - t0) * p.d * 2));
-            for (int32_t tt = t0; tt < t1;) {
-                const int32_t pg = pt[tt / p.page_size];
-                const int32_t n = min(t1, (tt / p.page_size + 1) * p.page_size) - tt;
-                const int64_t off = kv_offset(p, t.layer, pg, t.a1, tt % p.page_size);
-                const uint32_t bytes = (uint32_t)(n * p.d * 2);
-                bulk_g2s(dst + (size_t)(tt - t0) * p.d * 2, p.k_pool + off, bytes, &c.sc->full[s], pol);
-                bulk_g2s(dst + ((size_t)tps + (tt - t0)) * p.d * 2, p.v_pool + off, bytes, &c.sc->full[s], pol);
-                tt += n;
+        for (int32_t blk = r.blo; blk < r.bhi; ++blk) {
+            const int32_t tok0 = blk * kAttnBlock;
+            const int32_t pg = pt[tok0 / p.page_size];
+            const int32_t row0 =
+                (int32_t)((((int64_t)t.layer * p.num_pages + pg) * p.nkv + t.a1) * p.page_size + tok0 % p.page_size);
+            for (int j = 0; j < kAttnBlock / ts; ++j) {
+                uint32_t s;
+                if (!acquire_slot(c, &s)) return false;
+                uint8_t *dst = c.ring + (size_t)s * slot_bytes;
+                mbar_arrive_expect_tx(&c.sc->full[s], (uint32_t)(2 * halves * ts * 128));
+                for (int h = 0; h < halves; ++h) {
+                    tma_load_2d(dst + (size_t)h * ts * 128, p.kv_maps[0], h * 64, row0 + j * ts, &c.sc->full[s], pol);
+                    tma_load_2d(dst + (size_t)(halves + h) * ts * 128, p.kv_maps[1], h * 64, row0 + j * ts,
+                                &c.sc->full[s], pol);
+                }
+                ++issued;
             }
-            ++issued;
         }
         return true;
     }
@@ -364,8 +382,8 @@ struct Producer {
                 if (!acquire_slot(c, &s)) return false;
                 int lt;
                 const int map = weight_map(p, t.op, t.layer, tile, m, &lt);
-                mbar_arrive_expect_tx(&c.sc->full[s], (uint32_t)p.slot_bytes);
-                tma_load_2d(c.ring + (size_t)s * p.slot_bytes, tmap(p, map), kc * kTcTileK, lt * kTcTileM,
+                mbar_arrive_expect_tx(&c.sc->full[s], slot_bytes);
+                tma_load_2d(c.ring + (size_t)s * slot_bytes, tmap(p, map), kc * kTcTileK, lt * kTcTileM,
                             &c.sc->full[s], pol);
                 ++issued;
             }
@@ -396,6 +414,8 @@ __device__ void producer_role(const Ctx &c, const Task *q, int nt) {
     if ((threadIdx.x & 31) != 0) return;
     Producer pr;
     pr.pol = policy_evict_first();
+    pr.ns = (uint32_t)c.p->num_slots;
+    pr.slot_bytes = (uint32_t)c.p->slot_bytes;
     for (int i = 0; i < nt; ++i) {
         const Task t = q[i];
         if (!task_active(*c.p, t)) continue;
@@ -459,20 +479,23 @@ __device__ void scheduler_loop(const Ctx &c, const Task *q, int nt, ActProducer 
         if (use_events && task_active(p, t) && t.wait_ev != kNoEvent) {
             const uint32_t *ctr = p.ctl + t.wait_ev;
             if (ld_acquire_gpu(ctr) < t.wait_count) {
-                uint64_t t0 = globaltimer_ns();
-                for (uint32_t it = 1;; ++it) {
+                const uint64_t t0 = globaltimer_ns();
+                uint64_t next = t0 + kAbortCheckNs;
+                for (;;) {
                     if (ld_acquire_gpu(ctr) >= t.wait_count) break;
-                    if ((it & 7u) == 0) {
+                    const uint64_t now = globaltimer_ns();
+                    if (now >= next) {
                         if (local_abort(c) || global_abort(p)) {
                             set_local_abort(c);
                             st_release_cta(&c.sc->ready, kReadyAbort);
                             return;
                         }
-                        if (globaltimer_ns() - t0 > p.timeout_ns) {
+                        if (now - t0 > p.timeout_ns) {
                             record_error(c, 4, SITE_EVENT_WAIT, t.wait_ev);
                             st_release_cta(&c.sc->ready, kReadyAbort);
                             return;
                         }
+                        next = now + kAbortCheckNs;
                     }
                 }
             }
@@ -571,22 +594,35 @@ __device__ __forceinline__ float dot8(const uint4 w, const float *x) {
 }
 
 struct Consumer {
+    uint32_t ns = 0;         // ring slots and slot size (kept in registers)
+    uint32_t slot_bytes = 0;
     uint32_t consumed = 0;   // weight / KV ring slots
     uint32_t aconsumed = 0;  // activation ring slots (batched path)
     uint32_t seg = 0;        // accumulator segments (batched path)
     int ct, wc, lane;  // compute-thread index, compute-warp index, lane
     uint32_t red_buf = 0;
     bool tracing = false;
-    uint64_t full_wait_ns = 0;
+    uint64_t full_wait_ns = 0;  // traced: waits for filled weight / KV slots
+    uint64_t act_wait_ns = 0;   // traced (batched): waits for activation tiles
+    uint64_t acc_wait_ns = 0;   // traced (batched): waits for a free TMEM accumulator
 
     // A failed wait (abort or timeout) marks the CTA aborted but keeps the
     // control flow: all compute warps must reach the same named barriers, so
     // they leave only together, at a task boundary.
     __device__ uint32_t wait_slot(const Ctx &c) {
-        const uint32_t s = consumed % (uint32_t)c.p->num_slots;
-        const uint32_t round = consumed / (uint32_t)c.p->num_slots;
+        const uint32_t s = consumed % ns;
+        const uint32_t round = consumed / ns;
         const uint64_t t0 = tracing ? globaltimer_ns() : 0;
         wait_mbar(c, &c.sc->full[s], round & 1u, SITE_FULL_WAIT);
+        if (tracing) full_wait_ns += globaltimer_ns() - t0;
+        return s;
+    }
+
+    // Wait for ring slot number k (k = consumed + j for lookahead).
+    __device__ uint32_t wait_slot_at(const Ctx &c, uint32_t k) {
+        const uint32_t s = k % ns;
+        const uint64_t t0 = tracing ? globaltimer_ns() : 0;
+        wait_mbar(c, &c.sc->full[s], (k / ns) & 1u, SITE_FULL_WAIT);
         if (tracing) full_wait_ns += globaltimer_ns() - t0;
         return s;
     }
@@ -614,7 +650,7 @@ struct Consumer {
     __device__ void run_matvec(const Ctx &c, const Task &t) {
         const KParams &p = *c.p;
         const int op = t.op;
-        const MvGeom &g = p.mv[op];
+        const MvGeom g = p.mv[op];
         const int32_t nchunk = g.K / 8;
         const LayerW &lw = p.layers[t.layer];
         const int32_t token = p.tokens[0];
@@ -693,7 +729,7 @@ struct Consumer {
                 if (ks < g.ksplit) {
                     const uint32_t s = wait_slot(c);
                     const int32_t pw8 = min(g.kc, g.K - ks * g.kc) >> 3;  // chunks per row in this piece
-                    const uint4 *base = reinterpret_cast<const uint4 *>(c.ring + (size_t)s * p.slot_bytes) + ct;
+                    const uint4 *base = reinterpret_cast<const uint4 *>(c.ring + (size_t)s * slot_bytes) + ct;
                     // the slot goes back to the producer as soon as its data is in registers
                     uint4 w[8];
 #pragma unroll
@@ -743,7 +779,7 @@ struct Consumer {
     // them back and run the fused epilogue; the other compute warps idle.
     __device__ void run_gemm(const Ctx &c, const Task &t) {
         const KParams &p = *c.p;
-        const TcGeom &g = p.tcg[t.op];
+        const TcGeom g = p.tcg[t.op];
         const int mats = (t.op == OP_GU) ? 2 : 1;
         const int32_t t0 = t.a0 / g.kchunks, t1 = (t.a1 - 1) / g.kchunks;
         const bool issuer = (wc == 0 && lane == 0);
@@ -759,29 +795,38 @@ struct Consumer {
     __device__ void mma_issuer(const Ctx &c, const Task &t, const TcGeom &g, int mats, int32_t t0, int32_t t1) {
         const KParams &p = *c.p;
         SmemCtl *sc = c.sc;
-        const uint32_t ns = (uint32_t)p.num_slots, nas = (uint32_t)p.num_aslots;
+        const uint32_t nas = (uint32_t)p.num_aslots;
         uint32_t sg = seg;
         for (int32_t tile = t0; tile <= t1; ++tile, ++sg) {
             const int32_t klo = (tile == t0) ? t.a0 % g.kchunks : 0;
             const int32_t khi = (tile == t1) ? (t.a1 - 1) % g.kchunks + 1 : g.kchunks;
             const uint32_t ab = sg & 1u, use = sg >> 1;
+            uint64_t t0 = tracing ? globaltimer_ns() : 0;
             if (!wait_mbar(c, &sc->acc_empty[ab], (use & 1u) ^ 1u, SITE_ACC_WAIT)) return;
+            if (tracing) acc_wait_ns += globaltimer_ns() - t0;
             tc_fence_after();
             const uint32_t dcol = sc->tmem_base + ab * 4u * (uint32_t)p.npad;
             for (int32_t k = klo; k < khi; ++k) {
                 uint32_t ws[2] = {0u, 0u};
+                if (tracing) t0 = globaltimer_ns();
                 for (int m = 0; m < mats; ++m) {
                     ws[m] = consumed % ns;
                     if (!wait_mbar(c, &sc->full[ws[m]], (consumed / ns) & 1u, SITE_FULL_WAIT)) return;
                     ++consumed;
                 }
+                if (tracing) {
+                    const uint64_t t1 = globaltimer_ns();
+                    full_wait_ns += t1 - t0;
+                    t0 = t1;
+                }
                 const uint32_t as = aconsumed % nas;
                 if (!wait_mbar(c, &sc->afull[as], (aconsumed / nas) & 1u, SITE_FULL_WAIT)) return;
                 ++aconsumed;
+                if (tracing) act_wait_ns += globaltimer_ns() - t0;
                 tc_fence_after();
                 const uint32_t abase = smem_u32(c.aring + (size_t)as * p.aslot_bytes);
                 for (int m = 0; m < mats; ++m) {
-                    const uint32_t wbase = smem_u32(c.ring + (size_t)ws[m] * p.slot_bytes);
+                    const uint32_t wbase = smem_u32(c.ring + (size_t)ws[m] * slot_bytes);
 #pragma unroll
                     for (int kk = 0; kk < kTcTileK / 16; ++kk)
                         umma_bf16(dcol + (uint32_t)(m * 2 * p.npad), umma_desc_sw128(wbase + kk * 32),
@@ -992,116 +1037,60 @@ struct Consumer {
     }
 
     // ---------------------------------------------------- attention task
-    // Scores, online-softmax update and value accumulation for ntok tokens
-    // whose K rows start at kp and V rows at vp (bf16 [ntok][d] in smem).
-    __device__ void attn_block(const Ctx &c, const uint16_t *kp, const uint16_t *vp, int32_t ntok, int G,
-                               float *o_acc, int npairs_mine) {
-        const KParams &p = *c.p;
-        const int d = p.d;
-        const int nck = d / 64;  // 16-byte chunks per lane
-        const int t_sub = lane >> 3, part = lane & 7;
-        SmemCtl *sc = c.sc;
-        // scores: 4 tokens per warp per pass, 8 lanes per token
-        for (int32_t base = 0; base < ntok; base += kComputeWarps * 4) {
-            const int32_t tok = base + wc * 4 + t_sub;
-            const bool valid = tok < ntok;
-            float acc[kMaxGroup];
-#pragma unroll
-            for (int g = 0; g < kMaxGroup; ++g) acc[g] = 0.f;
-            if (valid) {
-                for (int i = 0; i < nck; ++i) {
-                    const int chunk = part + 8 * ((i + t_sub) % nck);
-                    const uint4 kv = reinterpret_cast<const uint4 *>(kp + (size_t)tok * d)[chunk];
-                    const float kf[8] = {bf16_lo(kv.x), bf16_hi(kv.x), bf16_lo(kv.y), bf16_hi(kv.y),
-                                         bf16_lo(kv.z), bf16_hi(kv.z), bf16_lo(kv.w), bf16_hi(kv.w)};
-#pragma unroll
-                    for (int g = 0; g < kMaxGroup; ++g) {
-                        if (g < G) {
-                            const float4 qa = *reinterpret_cast<const float4 *>(&sc->q_s[g][chunk * 8]);
-                            const float4 qb = *reinterpret_cast<const float4 *>(&sc->q_s[g][chunk * 8 + 4]);
-                            float a = acc[g];
-                            a = fmaf(kf[0], qa.x, a); a = fmaf(kf[1], qa.y, a);
-                            a = fmaf(kf[2], qa.z, a); a = fmaf(kf[3], qa.w, a);
-                            a = fmaf(kf[4], qb.x, a); a = fmaf(kf[5], qb.y, a);
-                            a = fmaf(kf[6], qb.z, a); a = fmaf(kf[7], qb.w, a);
-                            acc[g] = a;
-                        }
-                    }
-                }
-            }
-#pragma unroll
-            for (int g = 0; g < kMaxGroup; ++g) {
-                float v = acc[g];
-                v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
-                v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
-                v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
-                if (g < G && valid && part == 0) sc->s_s[g][tok] = v;
-            }
-        }
-        compute_bar();
-        // online softmax: warp g owns head g
-        if (wc < G) {
-            const int g = wc;
-            float mx = -INFINITY;
-            for (int32_t tk = lane; tk < ntok; tk += 32) mx = fmaxf(mx, sc->s_s[g][tk]);
-            mx = warp_max(mx);
-            const float m_old = sc->att_m[g];
-            const float m_new = fmaxf(m_old, mx);
-            float sum = 0.f;
-            for (int32_t tk = lane; tk < ntok; tk += 32) {
-                const float e = expf(sc->s_s[g][tk] - m_new);
-                sc->s_s[g][tk] = e;
-                sum += e;
-            }
-            sum = warp_sum(sum);
-            if (lane == 0) {
-                const float alpha = expf(m_old - m_new);  // 0 when m_old = -inf
-                sc->att_alpha[g] = alpha;
-                sc->att_l[g] = sc->att_l[g] * alpha + sum;
-                sc->att_m[g] = m_new;
-            }
-        }
-        compute_bar();
-        // o = o * alpha + sum_t p_t v_t; this thread owns pairs ct + 256 k
-        const int half = d / 2;
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            if (k < npairs_mine) {
-                const int pr = ct + kComputeThreads * k;
-                const int g = pr / half, e = (pr % half) * 2;
-                float o0 = o_acc[2 * k] * sc->att_alpha[g], o1 = o_acc[2 * k + 1] * sc->att_alpha[g];
-                for (int32_t tk = 0; tk < ntok; ++tk) {
-                    const uint32_t v2 = *reinterpret_cast<const uint32_t *>(vp + (size_t)tk * d + e);
-                    const float pw = sc->s_s[g][tk];
-                    o0 = fmaf(pw, bf16_lo(v2), o0);
-                    o1 = fmaf(pw, bf16_hi(v2), o1);
-                }
-                o_acc[2 * k] = o0;
-                o_acc[2 * k + 1] = o1;
-            }
-        }
+    // One (sequence, kv head, context split) task.  The G query heads of the
+    // kv head are split into bf16 high and low parts (2G MMA columns), so the
+    // bf16 tensor-core products keep about 16 significant bits of q and of
+    // the softmax weights.  Per 64-token block of the cache:
+    //   scores  S^T[tok][2G] = K[tok][d] Q^T     (warps 0..3, 16 tokens each)
+    //   online softmax per head                  (warp g for head g)
+    //   O^T[d][2G] += V^T[d][tok] P^T[tok][2G]   (warp w for rows 16w..16w+15)
+    // with mma.sync m16n8k16 (bf16 in, fp32 accumulate) on K/V tiles that the
+    // producer laid out 128-byte swizzled, so every ldmatrix is conflict-free.
+
+    // Shared-memory address of element e of token `tok` (0..63) of the K
+    // (kv = 0) or V (kv = 1) tile of a block held in slots sb0 (tokens
+    // [0, ts)) and sb1 (tokens [ts, 64)); ts = 1 << ts_log2.  Shifts and a
+    // select only: no local-memory array, no integer division.
+    __device__ static __forceinline__ uint32_t kv_elem(uint32_t sb0, uint32_t sb1, int ts_log2, int halves, int kv,
+                                                       int tok, int e) {
+        const int ti = tok & ((1 << ts_log2) - 1), h = e >> 6, ch = (e & 63) >> 3;
+        return ((tok >> ts_log2) ? sb1 : sb0) +
+               (uint32_t)((((kv * halves + h) * 128) << ts_log2) + ti * 128 + ((ch ^ (ti & 7)) << 4) + (e & 7) * 2);
     }
 
     __device__ void run_attn(const Ctx &c, const Task &t) {
         const KParams &p = *c.p;
         SmemCtl *sc = c.sc;
-        const int d = p.d, half = d / 2;
-        const int G = p.nq / p.nkv;
+        const int d = p.d, half = d / 2, halves = d / 64, nks = d / 16;
+        const int G = p.nq / p.nkv, NT = (2 * G + 7) / 8;
         const int b = t.a0, kvh = t.a1, S = t.a3;
         const AttnRange r = attn_range(p, t);
         const float *qkv = p.qkv + (int64_t)b * p.qkv_rows;
         const float2 *rope = p.rope + (int64_t)r.pos * half;
         const float scale = rsqrtf((float)d);
+        const int ts = p.attn_ts, nsl = kAttnBlock / ts, ts_log2 = (ts == 64) ? 6 : 5;
 
-        // RoPE'd, pre-scaled queries of the G heads sharing this kv head
+        // RoPE'd, pre-scaled queries of the G heads sharing this kv head, in
+        // fp32 and split into bf16 high / low parts (rows G..2G-1 the low parts)
         for (int idx = ct; idx < G * half; idx += kComputeThreads) {
             const int g = idx / half, i = idx % half;
             const float *qh = qkv + (int64_t)(kvh * G + g) * d;
             const float a = __ldcg(qh + i), bb = __ldcg(qh + i + half);
             const float2 cs = rope[i];
-            sc->q_s[g][i] = (a * cs.x - bb * cs.y) * scale;
-            sc->q_s[g][i + half] = (a * cs.y + bb * cs.x) * scale;
+            const float q0 = (a * cs.x - bb * cs.y) * scale, q1 = (a * cs.y + bb * cs.x) * scale;
+            sc->q_s[g][i] = q0;
+            sc->q_s[g][i + half] = q1;
+            const uint16_t h0 = f32_to_bf16_bits(q0), h1 = f32_to_bf16_bits(q1);
+            sc->q_hl[g][i] = h0;
+            sc->q_hl[g][i + half] = h1;
+            sc->q_hl[G + g][i] = f32_to_bf16_bits(q0 - __uint_as_float((uint32_t)h0 << 16));
+            sc->q_hl[G + g][i + half] = f32_to_bf16_bits(q1 - __uint_as_float((uint32_t)h1 << 16));
         }
+        // MMA columns past 2G stay zero
+        for (int idx = ct; idx < (8 * NT - 2 * G) * kQhlStride; idx += kComputeThreads)
+            sc->q_hl[2 * G + idx / kQhlStride][idx % kQhlStride] = 0;
+        for (int idx = ct; idx < (8 * NT - 2 * G) * kPhlStride; idx += kComputeThreads)
+            sc->p_hl[2 * G + idx / kPhlStride][idx % kPhlStride] = 0;
         if (r.has_new) {
             // K/V of the new token: RoPE on k, round to bf16, append to the cache
             const float *kh = qkv + (int64_t)p.nq * d + (int64_t)kvh * d;
@@ -1130,31 +1119,162 @@ struct Consumer {
         }
         compute_bar();
 
-        const int npairs = G * half;
-        const int mine = (ct < npairs) ? (npairs - ct + kComputeThreads - 1) / kComputeThreads : 0;
-        float o_acc[4] = {0.f, 0.f, 0.f, 0.f};  // up to 2 pairs per thread (G*d/2 <= 512)
-        for (int32_t t0 = r.lo; t0 < r.cend; t0 += p.tps) {
-            const int32_t ntok = min(r.cend, t0 + p.tps) - t0;
-            const uint32_t s = wait_slot(c);
-            const uint16_t *kp = reinterpret_cast<const uint16_t *>(c.ring + (size_t)s * p.slot_bytes);
-            attn_block(c, kp, kp + (size_t)p.tps * d, ntok, G, o_acc, mine);
-            release_slot(c, s);
-            compute_bar();  // scores buffer reused by the next block
+        const uint32_t qb = smem_u32(&sc->q_hl[0][0]);  // B operand (Q^T) of the score MMAs
+        // hi/lo column pairing of the MMA C fragment: column n holds the high
+        // part of head n (n < G) or the low part of head n - G
+        const int tr = lane >> 2, cq = lane & 3;
+        const int partner = (G == 8) ? 0 : (G >= 2 ? G / 2 : 0);  // lane distance to the low-part column
+        const bool head_lane = (G == 8) || (G == 1 ? cq == 0 : cq < G / 2);
+        float oacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+
+        for (int32_t blk = r.blo; blk < r.bhi; ++blk) {
+            const uint64_t tb0 = tracing ? globaltimer_ns() : 0;
+            const uint32_t sid0 = wait_slot_at(c, consumed);
+            const uint32_t sid1 = (nsl == 2) ? wait_slot_at(c, consumed + 1u) : sid0;
+            const uint32_t sb0 = smem_u32(c.ring + (size_t)sid0 * slot_bytes);
+            const uint32_t sb1 = smem_u32(c.ring + (size_t)sid1 * slot_bytes);
+            const int32_t tok0 = blk * kAttnBlock;
+            // scores of tokens 16 wc .. 16 wc + 15
+            if (wc < 4) {
+                float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    if (ks < nks) {
+                        uint32_t a[4], qf[2];
+                        ldsm_x4(a, kv_elem(sb0, sb1, ts_log2, halves, 0, 16 * wc + (lane & 15), ks * 16 + (lane >> 4) * 8));
+#pragma unroll
+                        for (int nt = 0; nt < 2; ++nt) {
+                            if (nt < NT) {
+                                ldsm_x2(qf, qb + (uint32_t)((((lane & 7) + 8 * nt) * kQhlStride + ks * 16 +
+                                                             ((lane >> 3) & 1) * 8) * 2));
+                                mma_bf16_16816(sacc[nt], a, qf);
+                            }
+                        }
+                    }
+                }
+                // sum the high and low parts, mask tokens past the cached context
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float v = sacc[0][i];
+                    if (G == 8) v += sacc[1][i];
+                    else if (G == 1) v = (i & 1) ? 0.f : sacc[0][i] + sacc[0][i + 1];
+                    else v += __shfl_xor_sync(0xFFFFFFFFu, v, partner);
+                    const int tok = 16 * wc + tr + (i >> 1) * 8;
+                    const int head = (G == 1) ? 0 : 2 * cq + (i & 1);
+                    const bool live = head_lane && (G != 1 || (i & 1) == 0);
+                    if (live) sc->s_s[head][tok] = (tok0 + tok < r.pos) ? v : -INFINITY;
+                }
+            }
+            compute_bar();
+            const uint64_t tb1 = tracing ? globaltimer_ns() : 0;
+            // online softmax, warp g for head g: weights as bf16 high / low parts
+            if (wc < G) {
+                const int g = wc;
+                const float s0 = sc->s_s[g][lane], s1 = sc->s_s[g][lane + 32];
+                const float m_old = sc->att_m[g];
+                const float m_new = fmaxf(m_old, warp_max(fmaxf(s0, s1)));
+                const float p0 = (s0 == -INFINITY) ? 0.f : expf(s0 - m_new);
+                const float p1 = (s1 == -INFINITY) ? 0.f : expf(s1 - m_new);
+                const float sum = warp_sum(p0 + p1);
+                const uint16_t h0 = f32_to_bf16_bits(p0), h1 = f32_to_bf16_bits(p1);
+                sc->p_hl[g][lane] = h0;
+                sc->p_hl[g][lane + 32] = h1;
+                sc->p_hl[G + g][lane] = f32_to_bf16_bits(p0 - __uint_as_float((uint32_t)h0 << 16));
+                sc->p_hl[G + g][lane + 32] = f32_to_bf16_bits(p1 - __uint_as_float((uint32_t)h1 << 16));
+                if (lane == 0) {
+                    const float alpha = (m_old == -INFINITY) ? 0.f : expf(m_old - m_new);
+                    sc->att_alpha[g] = alpha;
+                    sc->att_l[g] = sc->att_l[g] * alpha + sum;
+                    sc->att_m[g] = m_new;
+                }
+            }
+            compute_bar();
+            const uint64_t tb2 = tracing ? globaltimer_ns() : 0;
+            // O^T rows 16 wc .. 16 wc + 15: rescale, then add V^T P^T
+            if (wc < nks) {
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int col = nt * 8 + 2 * cq + (i & 1);
+                        if (nt < NT && col < 2 * G) oacc[nt][i] *= sc->att_alpha[col % G];
+                    }
+                const uint32_t pb = smem_u32(&sc->p_hl[0][0]);
+#pragma unroll
+                for (int k2 = 0; k2 < kAttnBlock / 16; ++k2) {
+                    uint32_t a[4];
+                    const int q = lane >> 3;
+                    ldsm_x4_trans(a, kv_elem(sb0, sb1, ts_log2, halves, 1, k2 * 16 + (q >> 1) * 8 + (lane & 7),
+                                             16 * wc + (q & 1) * 8));
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        if (nt < NT) {
+                            uint32_t bq[2];
+                            ldsm_x2(bq, pb + (uint32_t)((((lane & 7) + 8 * nt) * kPhlStride + k2 * 16 +
+                                                         ((lane >> 3) & 1) * 8) * 2));
+                            mma_bf16_16816(oacc[nt], a, bq);
+                        }
+                    }
+                }
+            }
+            compute_bar();  // the block's slots, scores and weights are free
+            if (ct == 0) {
+                const uint32_t na = p.tc ? 1u : (uint32_t)kComputeWarps;
+                mbar_arrive_n(&sc->empty[sid0], na);
+                if (nsl == 2) mbar_arrive_n(&sc->empty[sid1], na);
+            }
+            consumed += (uint32_t)nsl;
+            if (tracing) {
+                act_wait_ns += tb1 - tb0;            // slot waits + scores
+                acc_wait_ns += globaltimer_ns() - tb2;  // value sums
+            }
         }
         if (r.has_new) {
-            attn_block(c, sc->knew, sc->vnew, 1, G, o_acc, mine);
+            // the new token, from shared memory: one more online-softmax step
+            if (wc < G) {
+                const int g = wc;
+                float sdot = 0.f;
+                for (int e = lane; e < d; e += 32) sdot = fmaf(sc->q_s[g][e], __uint_as_float((uint32_t)sc->knew[e] << 16), sdot);
+                sdot = warp_sum(sdot);
+                if (lane == 0) {
+                    const float m_old = sc->att_m[g], m_new = fmaxf(m_old, sdot);
+                    const float alpha = (m_old == -INFINITY) ? 0.f : expf(m_old - m_new);
+                    const float pn = expf(sdot - m_new);
+                    sc->att_alpha[g] = alpha;
+                    sc->att_pnew[g] = pn;
+                    sc->att_l[g] = sc->att_l[g] * alpha + pn;
+                    sc->att_m[g] = m_new;
+                }
+            }
+            compute_bar();
+            if (wc < nks) {
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int col = nt * 8 + 2 * cq + (i & 1);
+                        if (nt < NT && col < 2 * G) {
+                            const int e = 16 * wc + tr + (i >> 1) * 8;
+                            const float vn = __uint_as_float((uint32_t)sc->vnew[e] << 16);
+                            oacc[nt][i] = oacc[nt][i] * sc->att_alpha[col % G] + (col < G ? sc->att_pnew[col] * vn : 0.f);
+                        }
+                    }
+            }
             compute_bar();
         }
-        // partial result of this split: unnormalised o, running max, sum
+        // partial result of this split: unnormalised o (high + low columns), running max, sum
         const int64_t pidx = (((int64_t)b * p.nkv + kvh) * S + t.a2) * G;
+        if (wc < nks) {
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            if (k < mine) {
-                const int pr = ct + kComputeThreads * k;
-                const int g = pr / half, e = (pr % half) * 2;
-                float *dst = p.attn_part + (pidx + g) * (d + 2);
-                dst[e] = o_acc[2 * k];
-                dst[e + 1] = o_acc[2 * k + 1];
+            for (int i = 0; i < 4; ++i) {
+                float v = oacc[0][i];
+                if (G == 8) v += oacc[1][i];
+                else if (G == 1) v = (i & 1) ? 0.f : oacc[0][i] + oacc[0][i + 1];
+                else v += __shfl_xor_sync(0xFFFFFFFFu, v, partner);
+                const int e = 16 * wc + tr + (i >> 1) * 8;
+                const int head = (G == 1) ? 0 : 2 * cq + (i & 1);
+                const bool live = head_lane && (G != 1 || (i & 1) == 0);
+                if (live) p.attn_part[(pidx + head) * (d + 2) + e] = v;
             }
         }
         if (ct < G) {
@@ -1194,9 +1314,10 @@ struct Consumer {
                 if (lane == 0) sc->att_inv_l[g] = 1.f / Ls;
             }
             compute_bar();
+            const int npairs = G * half;  // output pairs: (head, even column)
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
-                if (k < mine) {
+                if (ct + kComputeThreads * k < npairs) {
                     const int pr = ct + kComputeThreads * k;
                     const int g = pr / half, e = (pr % half) * 2;
                     const float *src = p.attn_part + (pbase + g) * (d + 2) + e;
@@ -1235,6 +1356,8 @@ template <int MAXCH>
 __device__ void compute_role(const Ctx &c, const Task *q, int nt) {
     const KParams &p = *c.p;
     Consumer cs;
+    cs.ns = (uint32_t)p.num_slots;
+    cs.slot_bytes = (uint32_t)p.slot_bytes;
     cs.ct = threadIdx.x - 64;
     cs.wc = cs.ct >> 5;
     cs.lane = threadIdx.x & 31;
@@ -1269,7 +1392,9 @@ __device__ void compute_role(const Ctx &c, const Task *q, int nt) {
         if (tr) {
             tr[2] = globaltimer_ns();
             tr[3] = cs.full_wait_ns;
-            cs.full_wait_ns = 0;
+            tr[6] = cs.act_wait_ns;
+            tr[7] = cs.acc_wait_ns;
+            cs.full_wait_ns = cs.act_wait_ns = cs.acc_wait_ns = 0;
         }
         if (aborted) return;
         if (t.op != OP_ATTN && p.only_op < 0 && t.signal_ev != kNoEvent && cs.ct == 0) {

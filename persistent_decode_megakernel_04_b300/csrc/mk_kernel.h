@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/mk.h"
 #include "mk_types.h"
 
 namespace mk {
@@ -16,7 +17,9 @@ constexpr int kThreads = (2 + kComputeWarps) * 32;  // 320
 constexpr int kMaxSlots = 16;
 constexpr int kMaxGroup = 8;      // q heads per kv head
 constexpr int kMaxHeadDim = 128;
-constexpr int kMaxTps = 128;      // KV tokens per ring slot
+constexpr int kAttnBlock = 64;    // cached tokens per attention block (one aligned run of a page)
+constexpr int kQhlStride = kMaxHeadDim + 8;  // bf16 row stride of the split queries (conflict-free ldmatrix)
+constexpr int kPhlStride = kAttnBlock + 8;   // bf16 row stride of the split softmax weights
 constexpr int kMaxResid = 512;    // residual rows prefetched per matvec task
 constexpr int kMaxASlots = 8;     // activation ring slots (batched path)
 
@@ -47,7 +50,7 @@ struct KParams {
     const Task *tasks;
     const int32_t *queue_off;
     MvGeom mv[OP_COUNT];
-    int32_t slot_bytes, num_slots, tps, attn_splits;
+    int32_t slot_bytes, num_slots, attn_ts, attn_splits;  // attn_ts: KV tokens per ring slot
     int32_t l2_prefetch_bytes;
     // launch mode
     int32_t only_op;     // -1: every task (persistent mode); else one operator of one layer
@@ -57,6 +60,9 @@ struct KParams {
     // optional task trace: [num_ctas][trace_stride][8] globaltimer stamps
     uint64_t *trace;
     int32_t trace_stride;
+    // TMA maps of the K and V pools seen as [L*num_pages*nkv*page_size][d]
+    // bf16 rows, boxes of 64 columns x attn_ts rows, 128-byte swizzled
+    alignas(64) uint8_t kv_maps[2][128];
     // batched (tensor-core) path
     int32_t tc;              // nonzero: projections run as tcgen05 tiles
     int32_t npad;            // MMA N: batch rounded up to 16
@@ -88,6 +94,9 @@ cudaError_t launch_megakernel(const KParams &p, int variant, int grid, size_t sm
                               cudaStream_t stream);
 cudaError_t megakernel_max_active(int variant, size_t smem, int *blocks_per_sm);
 cudaError_t megakernel_set_smem(int variant, size_t smem);
+
+// Host: TMA maps of the K and V pools (KParams::kv_maps) for tiles of ts tokens.
+bool encode_kv_maps(KParams &k, const mk_model_cfg &c, const mk_kv_cache &kv, int32_t ts);
 
 cudaError_t launch_rope_table(float2 *rope, int32_t max_seq, int32_t d, float theta, cudaStream_t stream);
 cudaError_t launch_greedy_next(const float *logits, int32_t B, int32_t V, int32_t *tokens, int32_t *positions,

@@ -181,6 +181,7 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_model_cfg *cfg, const mk_we
     k.lm_head = static_cast<const uint16_t *>(w->lm_head);
     k.final_norm = static_cast<const uint16_t *>(w->final_norm);
     k.layers = reinterpret_cast<const LayerW *>(scratch + o_layers);
+    if (!encode_kv_maps(k, c, *kv, g.tps)) return MK_ERR_INVALID;
     k.k_pool = static_cast<uint16_t *>(kv->k_pool);
     k.v_pool = static_cast<uint16_t *>(kv->v_pool);
     k.page_table = kv->page_table;
@@ -204,7 +205,7 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_model_cfg *cfg, const mk_we
     for (int i = 0; i < OP_COUNT; ++i) k.mv[i] = g.mv[i];
     k.slot_bytes = g.slot_bytes;
     k.num_slots = g.num_slots;
-    k.tps = g.tps;
+    k.attn_ts = g.tps;
     k.attn_splits = g.attn_splits;
     k.l2_prefetch_bytes = g.l2_prefetch_bytes;
     k.only_op = -1;

@@ -59,7 +59,8 @@ mk_status check_cfg(const mk_model_cfg &c) {
     if (c.hidden % 8 || c.ffn_dim % 8 || c.head_dim % 64) return MK_ERR_UNSUPPORTED;
     if (c.n_layers * 5 + 1 >= 0xFFFF) return MK_ERR_UNSUPPORTED;
     const int32_t group = c.n_q_heads / c.n_kv_heads;
-    if (group > 8 || c.head_dim > 128) return MK_ERR_UNSUPPORTED;
+    if (group > 8 || (group & (group - 1)) || c.head_dim > 128) return MK_ERR_UNSUPPORTED;
+    if (c.page_size % 64) return MK_ERR_UNSUPPORTED;  // attention reads aligned 64-token blocks of a page
     // a matvec input is held in registers: at most 16 row pieces of 2048 columns
     if (std::max({c.hidden, c.ffn_dim, c.n_q_heads * c.head_dim}) > 16 * kMvPiece) return MK_ERR_UNSUPPORTED;
     if (c.batch > kTcMaxBatch) return MK_ERR_UNSUPPORTED;  // one tcgen05 N tile holds the whole batch
@@ -116,7 +117,9 @@ mk_status build_plan(const mk_model_cfg &cfg, const mk_plan_options &opt, PlanTa
     g.attn_splits = S;
     g.slot_bytes = tc ? kTcTileM * kTcTileK * 2 : opt.slot_bytes;
     g.num_slots = opt.num_slots;
-    g.tps = std::min(128, g.slot_bytes / (2 * d * 2));
+    // KV tokens per ring slot: a 64-token attention block fills 1 or 2 slots
+    g.tps = (g.slot_bytes >= 2 * d * 2 * 64) ? 64 : 32;
+    if (g.slot_bytes < 2 * d * 2 * 32) return MK_ERR_INVALID;
     g.n_events = 5 * L + (tc ? 1 : 0);
     g.l2_prefetch_bytes = opt.l2_prefetch_kb * 1024;
     if (g.tps < 1) return MK_ERR_INVALID;

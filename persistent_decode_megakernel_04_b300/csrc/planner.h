@@ -13,7 +13,7 @@ struct PlanGeom {
     int32_t attn_splits = 0;
     int32_t slot_bytes = 0;
     int32_t num_slots = 0;
-    int32_t tps = 0;  // KV tokens per ring slot
+    int32_t tps = 0;  // KV tokens per ring slot (divides the 64-token attention block)
     int32_t n_events = 0;
     int32_t l2_prefetch_bytes = 0;
     MvGeom mv[OP_COUNT] = {};

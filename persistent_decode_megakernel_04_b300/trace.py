@@ -27,7 +27,8 @@ def phases(tasks, trace: np.ndarray) -> list:
     last end, mean compute-side data wait and mean producer ring-full wait,
     all in microseconds relative to the earliest stamp of the step."""
     t0 = int(trace[..., 1][trace[..., 1] > 0].min())
-    acc = defaultdict(lambda: {"rel": [], "start": [], "end": [], "wait": [], "ring_full": [], "dur": []})
+    acc = defaultdict(lambda: {"rel": [], "start": [], "end": [], "wait": [], "ring_full": [], "dur": [],
+                               "act_wait": [], "acc_wait": []})
     for cta, q in _by_cta(tasks).items():
         for i, t in enumerate(q):
             e = trace[cta, i]
@@ -40,6 +41,8 @@ def phases(tasks, trace: np.ndarray) -> list:
             a["dur"].append((int(e[2]) - int(e[1])) / 1e3)
             a["wait"].append(int(e[3]) / 1e3)
             a["ring_full"].append(int(e[5]) / 1e3)
+            a["act_wait"].append(int(e[6]) / 1e3)
+            a["acc_wait"].append(int(e[7]) / 1e3)
     rows = []
     for (layer, op), a in sorted(acc.items(), key=lambda kv: min(kv[1]["start"])):
         rel = [r for r in a["rel"] if r is not None]
@@ -49,6 +52,7 @@ def phases(tasks, trace: np.ndarray) -> list:
             "first_start_us": min(a["start"]), "last_end_us": max(a["end"]),
             "mean_task_us": float(np.mean(a["dur"])), "max_task_us": float(np.max(a["dur"])),
             "mean_data_wait_us": float(np.mean(a["wait"])), "mean_ring_full_us": float(np.mean(a["ring_full"])),
+            "mean_act_wait_us": float(np.mean(a["act_wait"])), "mean_acc_wait_us": float(np.mean(a["acc_wait"])),
         })
     return rows
 

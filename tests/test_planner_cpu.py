@@ -211,3 +211,19 @@ def test_batched_schedule_completes(name, B, num_ctas, seed):
     for l in range(m.n_layers):
         assert min(pos[(l, mk.OP_ATTN)]) > max(pos[(l, mk.OP_QKV)])
         assert min(pos[(l, mk.OP_DOWN)]) > max(pos[(l, mk.OP_GU)])
+
+
+@pytest.mark.parametrize("S", [1, 3, 18, 64])
+@pytest.mark.parametrize("pos", [0, 1, 63, 64, 65, 130, 4096, 4159])
+def test_attention_splits_cover_cached_blocks_once(S, pos):
+    """Attention reads the cached context [0, pos) in aligned 64-token blocks;
+    split s of S takes blocks [s*nb/S, (s+1)*nb/S) (the device's arithmetic),
+    so every cached token is read by exactly one split, and the last split
+    alone attends to the new token at pos."""
+    nb = (pos + 63) // 64
+    seen = []
+    for s in range(S):
+        seen += list(range(s * nb // S, (s + 1) * nb // S))
+    assert seen == list(range(nb))
+    covered = {t for b in seen for t in range(64 * b, 64 * b + 64) if t < pos}
+    assert covered == set(range(pos))
