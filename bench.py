@@ -190,7 +190,8 @@ def run_mk(args, wl):
     B = wl.batch
     max_seq = ((wl.prompt_len + args.warmup + args.steps + args.e2e_steps + 4 + 63) // 64) * 64
     weights = synth.device_weights(m, wl.seed, device=dev)
-    plan = mk.Plan(m, weights, batch=B, max_seq=max_seq)
+    popts = mk.mk_plan_options(tensor_cores=1) if args.tensor_cores else None
+    plan = mk.Plan(m, weights, batch=B, max_seq=max_seq, opts=popts)
     kv = mk.KVCache(m, B, max_seq, shuffle_seed=1, device=dev)
     logits = torch.empty((B, m.vocab), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -291,7 +292,7 @@ def run_mk(args, wl):
         # one more step with a tracing plan over the same weights and cache
         from persistent_decode_megakernel_04_b300 import trace as mktrace
 
-        topt = mk.mk_plan_options(trace=1)
+        topt = mk.mk_plan_options(trace=1, tensor_cores=1 if args.tensor_cores else 0)
         tplan = mk.Plan(m, weights, batch=B, max_seq=max_seq, opts=topt)
         tpos = h_pos.to(dev)
         for _ in range(2):
@@ -317,6 +318,7 @@ def run_mk(args, wl):
             "data": "synthetic (seeded random-init weights, random prompt ids)",
             "config": {"workload": args.workload, "model": m.name, "batch": B, "prompt_len": wl.prompt_len,
                        "context": "seeded paged cache" if seeded_context(wl) else "prefilled prompt",
+                       "projections": "tcgen05 tiles" if (B > 1 or args.tensor_cores) else "CUDA-core matvec",
                        "ctx_first_timed": ctx0, "ctx_last_timed": ctx0 + args.steps - 1,
                        "parallelism": f"replicas x{world}",
                        "l2": "no flush: ~15 GB of weights stream per step (> 126 MB L2)"},
@@ -352,6 +354,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prompt-len", type=int, default=0, help="override the workload's prompt length")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (sequences per step)")
+    ap.add_argument("--tensor-cores", action="store_true",
+                    help="run the projections as tcgen05 tiles at batch 1 too (default: CUDA-core matvecs)")
     ap.add_argument("--trace-out", default="", help="write a per-phase task trace of one extra step here")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

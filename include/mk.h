@@ -110,7 +110,9 @@ typedef struct {
                                        need one signal more than can ever arrive, so their
                                        bounded wait expires and the step reports MK_ERR_TIMEOUT */
     int32_t trace;         /* nonzero: record per-task timestamps (see mk_plan_trace) */
-    int32_t reserved[7];
+    int32_t tensor_cores;  /* 0: projections as CUDA-core matvecs at batch 1, tcgen05 tiles at
+                              batch >= 2; 1: tcgen05 tiles at every batch */
+    int32_t reserved[6];
 } mk_plan_options;
 
 typedef struct mk_plan mk_plan; /* opaque, library-owned */

@@ -581,6 +581,26 @@ __device__ __forceinline__ float warp_reduce16(const float (&a)[16], int lane) {
     return e;
 }
 
+// acc (two fp32 lanes, even and odd columns) += the 8 bf16 weights of w
+// times x: paired fp32 FMAs (fma.rn.f32x2), one per two weights.  The bf16
+// halves of each 32-bit word are widened exactly (shift, mask).
+__device__ __forceinline__ void dot8x2(uint64_t &acc, const uint4 w, const float *x) {
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        asm("{\n\t.reg .b64 wp, xp;\n\t"
+            "mov.b64 wp, {%1, %2};\n\t"
+            "mov.b64 xp, {%3, %4};\n\t"
+            "fma.rn.f32x2 %0, wp, xp, %0;\n\t}"
+            : "+l"(acc)
+            : "r"(ws[i] << 16), "r"(ws[i] & 0xFFFF0000u), "f"(x[2 * i]), "f"(x[2 * i + 1]));
+    }
+}
+
+__device__ __forceinline__ float sum_x2(uint64_t acc) {
+    return __uint_as_float((uint32_t)acc) + __uint_as_float((uint32_t)(acc >> 32));
+}
+
 __device__ __forceinline__ float dot8(const uint4 w, const float *x) {
     float a = bf16_lo(w.x) * x[0];
     a = fmaf(bf16_hi(w.x), x[1], a);
@@ -596,6 +616,7 @@ __device__ __forceinline__ float dot8(const uint4 w, const float *x) {
 struct Consumer {
     uint32_t ns = 0;         // ring slots and slot size (kept in registers)
     uint32_t slot_bytes = 0;
+    bool tcm = false;        // batched (tensor-core) plan
     uint32_t consumed = 0;   // weight / KV ring slots
     uint32_t aconsumed = 0;  // activation ring slots (batched path)
     uint32_t seg = 0;        // accumulator segments (batched path)
@@ -631,7 +652,7 @@ struct Consumer {
     // barrier also takes MMA commits, so it counts one arrival, made after
     // every compute warp is done with the slot.
     __device__ void release_slot(const Ctx &c, uint32_t s) {
-        if (c.p->tc) {
+        if (tcm) {
             compute_bar();
             if (ct == 0) mbar_arrive(&c.sc->empty[s]);
         } else {
@@ -644,9 +665,48 @@ struct Consumer {
     // ------------------------------------------------------- matvec task
     // Thread ct owns input chunks ct + 256 j (8 columns each), which are
     // exactly its chunk of row piece j; so every slot costs each thread one
-    // 128-bit shared load and 8 FMAs per row.  Row sums are kept per thread
-    // across the pieces of a row group and reduced once per group.
-    template <int MAXCH>
+    // 128-bit shared load and 4 paired FMAs per row.  Row sums are kept per
+    // thread across the pieces of a row group and reduced once per group.
+    // Inputs of at most two pieces (4096 columns) stay normalised in
+    // registers for the whole task; longer inputs are re-read per piece from
+    // L2 (one piece ahead) and normalised on the fly.
+    __device__ void load_piece(const KParams &p, const float *xin, const uint16_t *emb_row, const uint16_t *gain,
+                               float r, int32_t nchunk, int ks, float (&v)[8]) const {
+        const int32_t ch = ct + kComputeThreads * ks;
+        if (ch >= nchunk) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = 0.f;
+            return;
+        }
+        if (emb_row) {
+            const uint4 e = __ldg(reinterpret_cast<const uint4 *>(emb_row) + ch);
+            v[0] = bf16_lo(e.x); v[1] = bf16_hi(e.x); v[2] = bf16_lo(e.y); v[3] = bf16_hi(e.y);
+            v[4] = bf16_lo(e.z); v[5] = bf16_hi(e.z); v[6] = bf16_lo(e.w); v[7] = bf16_hi(e.w);
+        } else {
+            const float4 a = ld_cg_f4(xin + ch * 8), b = ld_cg_f4(xin + ch * 8 + 4);
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+        }
+        if (gain) {
+            const uint4 gv = __ldg(reinterpret_cast<const uint4 *>(gain) + ch);
+            v[0] *= r * bf16_lo(gv.x); v[1] *= r * bf16_hi(gv.x); v[2] *= r * bf16_lo(gv.y); v[3] *= r * bf16_hi(gv.y);
+            v[4] *= r * bf16_lo(gv.z); v[5] *= r * bf16_hi(gv.z); v[6] *= r * bf16_lo(gv.w); v[7] *= r * bf16_hi(gv.w);
+        }
+    }
+
+    // One ring slot: 8 rows (of which R are live) of the piece held in slot s.
+    __device__ __forceinline__ void mv_slot(const Ctx &c, int32_t pw8, int32_t R, const float (&xv)[8],
+                                            uint64_t (&acc2)[8]) {
+        const uint32_t s = wait_slot(c);
+        const uint4 *base = reinterpret_cast<const uint4 *>(c.ring + (size_t)s * slot_bytes) + ct;
+        // the slot goes back to the producer as soon as its data is in registers
+        uint4 w[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) w[r] = (ct < pw8 && r < R) ? base[r * pw8] : make_uint4(0u, 0u, 0u, 0u);
+        release_slot(c, s);
+#pragma unroll
+        for (int r = 0; r < 8; ++r) dot8x2(acc2[r], w[r], xv);
+    }
+
     __device__ void run_matvec(const Ctx &c, const Task &t) {
         const KParams &p = *c.p;
         const int op = t.op;
@@ -665,35 +725,26 @@ struct Consumer {
                                      : __ldcg(p.x + t.a0 + i);
         }
 
-        // input vector for this thread's chunks
-        float xr[MAXCH][8];
-        const bool from_embed = (op == OP_QKV && t.layer == 0);
+        const uint16_t *emb_row = (op == OP_QKV && t.layer == 0) ? p.embed + (int64_t)token * p.H : nullptr;
         const float *xin = (op == OP_O) ? p.attn_out : (op == OP_DOWN ? p.hbuf : p.x);
         const uint16_t *gain =
             op == OP_QKV ? lw.attn_norm : (op == OP_GU ? lw.mlp_norm : (op == OP_LM ? p.final_norm : nullptr));
+        const bool resident = g.ksplit <= 2;
+        float xr[2][8];
         float ss = 0.f;
 #pragma unroll
-        for (int j = 0; j < MAXCH; ++j) {
-            const int32_t ch = ct + kComputeThreads * j;
-            if (ch < nchunk) {
-                if (from_embed) {
-                    const uint4 e = __ldg(reinterpret_cast<const uint4 *>(p.embed + (int64_t)token * p.H) + ch);
-                    xr[j][0] = bf16_lo(e.x); xr[j][1] = bf16_hi(e.x);
-                    xr[j][2] = bf16_lo(e.y); xr[j][3] = bf16_hi(e.y);
-                    xr[j][4] = bf16_lo(e.z); xr[j][5] = bf16_hi(e.z);
-                    xr[j][6] = bf16_lo(e.w); xr[j][7] = bf16_hi(e.w);
-                } else {
-                    const float4 a = ld_cg_f4(xin + ch * 8), b = ld_cg_f4(xin + ch * 8 + 4);
-                    xr[j][0] = a.x; xr[j][1] = a.y; xr[j][2] = a.z; xr[j][3] = a.w;
-                    xr[j][4] = b.x; xr[j][5] = b.y; xr[j][6] = b.z; xr[j][7] = b.w;
-                }
+        for (int j = 0; j < 2; ++j) {
+            load_piece(p, xin, emb_row, nullptr, 1.f, nchunk, j < g.ksplit ? j : 1 << 20, xr[j]);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) ss = fmaf(xr[j][e], xr[j][e], ss);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) xr[j][e] = 0.f;
-            }
+            for (int e = 0; e < 8; ++e) ss = fmaf(xr[j][e], xr[j][e], ss);
         }
+        for (int j = 2; j < g.ksplit; ++j) {
+            float v[8];
+            load_piece(p, xin, emb_row, nullptr, 1.f, nchunk, j, v);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
+        }
+        float rn = 1.f;
         if (gain != nullptr) {
             // RMSNorm: r = 1/sqrt(mean(x^2) + eps), x-hat = g * x * r
             ss = warp_sum(ss);
@@ -702,44 +753,56 @@ struct Consumer {
             float tot = 0.f;
 #pragma unroll
             for (int w = 0; w < kComputeWarps; ++w) tot += c.sc->rms_part[w];
-            const float r = rsqrtf(tot / (float)g.K + p.eps);
+            rn = rsqrtf(tot / (float)g.K + p.eps);
             compute_bar();  // rms_part is reused by the next task
+            if (resident) {
 #pragma unroll
-            for (int j = 0; j < MAXCH; ++j) {
-                const int32_t ch = ct + kComputeThreads * j;
-                if (ch < nchunk) {
-                    const uint4 gv = __ldg(reinterpret_cast<const uint4 *>(gain) + ch);
-                    xr[j][0] *= r * bf16_lo(gv.x); xr[j][1] *= r * bf16_hi(gv.x);
-                    xr[j][2] *= r * bf16_lo(gv.y); xr[j][3] *= r * bf16_hi(gv.y);
-                    xr[j][4] *= r * bf16_lo(gv.z); xr[j][5] *= r * bf16_hi(gv.z);
-                    xr[j][6] *= r * bf16_lo(gv.w); xr[j][7] *= r * bf16_hi(gv.w);
+                for (int j = 0; j < 2; ++j) {
+                    const int32_t ch = ct + kComputeThreads * j;
+                    if (ch < nchunk) {
+                        const uint4 gv = __ldg(reinterpret_cast<const uint4 *>(gain) + ch);
+                        xr[j][0] *= rn * bf16_lo(gv.x); xr[j][1] *= rn * bf16_hi(gv.x);
+                        xr[j][2] *= rn * bf16_lo(gv.y); xr[j][3] *= rn * bf16_hi(gv.y);
+                        xr[j][4] *= rn * bf16_lo(gv.z); xr[j][5] *= rn * bf16_hi(gv.z);
+                        xr[j][6] *= rn * bf16_lo(gv.w); xr[j][7] *= rn * bf16_hi(gv.w);
+                    }
                 }
             }
         }
+        // streamed inputs: piece ks of the next slot, loaded one slot ahead
+        float xn[8];
+        if (!resident) load_piece(p, xin, emb_row, gain, rn, nchunk, 0, xn);
 
         const int lq = lane >> 2;  // row this lane holds after the reduce-scatter
+        // group geometry and outputs in registers (the ring's inline asm would
+        // otherwise force re-reads of the parameter block every slot)
+        const int32_t qb1 = p.nq * p.d, qb2 = qb1 + p.nkv * p.d, qb3 = p.qkv_rows;
+        float *const out_qkv = p.qkv, *const out_x = p.x, *const out_h = p.hbuf, *const out_logits = p.logits;
+        const uint16_t *const embed_row = p.embed + (int64_t)token * p.H;
         for (int32_t row = t.a0; row < t.a1;) {
-            const int32_t n = mv_group_rows(p, op, row, t.a1);
+            int32_t n = min(g.rpp, t.a1 - row);
+            if (op == OP_QKV) n = min(n, (row < qb1 ? qb1 : (row < qb2 ? qb2 : qb3)) - row);
             const int32_t R = n * g.row_mult;
-            float acc[8];
+            uint64_t acc2[8];
 #pragma unroll
-            for (int r = 0; r < 8; ++r) acc[r] = 0.f;
+            for (int r = 0; r < 8; ++r) acc2[r] = 0ull;
+            if (resident) {
 #pragma unroll
-            for (int ks = 0; ks < MAXCH; ++ks) {
-                if (ks < g.ksplit) {
-                    const uint32_t s = wait_slot(c);
-                    const int32_t pw8 = min(g.kc, g.K - ks * g.kc) >> 3;  // chunks per row in this piece
-                    const uint4 *base = reinterpret_cast<const uint4 *>(c.ring + (size_t)s * slot_bytes) + ct;
-                    // the slot goes back to the producer as soon as its data is in registers
-                    uint4 w[8];
+                for (int ks = 0; ks < 2; ++ks)
+                    if (ks < g.ksplit) mv_slot(c, min(g.kc, g.K - ks * g.kc) >> 3, R, xr[ks], acc2);
+            } else {
+                for (int ks = 0; ks < g.ksplit; ++ks) {
+                    float xc[8];
 #pragma unroll
-                    for (int r = 0; r < 8; ++r) w[r] = (ct < pw8 && r < R) ? base[r * pw8] : make_uint4(0u, 0u, 0u, 0u);
-                    release_slot(c, s);
-#pragma unroll
-                    for (int r = 0; r < 8; ++r) acc[r] += dot8(w[r], xr[ks]);
+                    for (int e = 0; e < 8; ++e) xc[e] = xn[e];
+                    load_piece(p, xin, emb_row, gain, rn, nchunk, ks + 1 < g.ksplit ? ks + 1 : 0, xn);
+                    mv_slot(c, min(g.kc, g.K - ks * g.kc) >> 3, R, xc, acc2);
                 }
             }
             // reduce-scatter of the 8 row sums over the warp: lane l ends with row l/4
+            float acc[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) acc[r] = sum_x2(acc2[r]);
             const float v = warp_reduce8(acc, lane);
             if ((lane & 3) == 0) c.sc->red[red_buf][wc][lq] = v;
             compute_bar();
@@ -756,15 +819,15 @@ struct Consumer {
                 if (has_resid) {
                     xo = resid_in_smem ? c.sc->resid[orow - t.a0]
                                        : ((op == OP_O && t.layer == 0)
-                                              ? __uint_as_float((uint32_t)p.embed[(int64_t)token * p.H + orow] << 16)
-                                              : __ldcg(p.x + orow));
+                                              ? __uint_as_float((uint32_t)embed_row[orow] << 16)
+                                              : __ldcg(out_x + orow));
                 }
                 switch (op) {
-                    case OP_QKV: p.qkv[orow] = tot; break;
+                    case OP_QKV: out_qkv[orow] = tot; break;
                     case OP_O:
-                    case OP_DOWN: p.x[orow] = xo + tot; break;
-                    case OP_GU: p.hbuf[orow] = tot / (1.f + expf(-tot)) * tot2; break;
-                    default: p.logits[orow] = tot; break;
+                    case OP_DOWN: out_x[orow] = xo + tot; break;
+                    case OP_GU: out_h[orow] = tot / (1.f + expf(-tot)) * tot2; break;
+                    default: out_logits[orow] = tot; break;
                 }
             }
             red_buf ^= 1u;
@@ -1358,6 +1421,7 @@ __device__ void compute_role(const Ctx &c, const Task *q, int nt) {
     Consumer cs;
     cs.ns = (uint32_t)p.num_slots;
     cs.slot_bytes = (uint32_t)p.slot_bytes;
+    cs.tcm = p.tc != 0;
     cs.ct = threadIdx.x - 64;
     cs.wc = cs.ct >> 5;
     cs.lane = threadIdx.x & 31;
@@ -1385,7 +1449,7 @@ __device__ void compute_role(const Ctx &c, const Task *q, int nt) {
         if (t.op == OP_ATTN) cs.run_attn(c, t);
         else if (t.op == OP_EMBED) cs.run_embed(c, t);
         else if (p.tc) cs.run_gemm(c, t);
-        else cs.run_matvec<MAXCH>(c, t);
+        else cs.run_matvec(c, t);
         // batched path: outputs are read by other CTAs' TMA (async proxy)
         if (p.tc) fence_proxy_async_global();
         const bool aborted = compute_bar_or(local_abort(c));  // every output row of the task is written
@@ -1557,14 +1621,7 @@ const void *kernel_ptr() {
     return reinterpret_cast<const void *>(&megakernel<MAXCH>);
 }
 
-const void *variant_ptr(int variant) {
-    switch (variant) {
-        case 2: return kernel_ptr<2>();
-        case 4: return kernel_ptr<4>();
-        case 8: return kernel_ptr<8>();
-        default: return kernel_ptr<16>();
-    }
-}
+const void *variant_ptr(int /*variant*/) { return kernel_ptr<2>(); }
 
 }  // namespace
 
@@ -1572,13 +1629,8 @@ size_t megakernel_smem_bytes(int32_t slot_bytes, int32_t num_slots, int32_t aslo
     return kRingOffset + (size_t)slot_bytes * num_slots + (size_t)aslot_bytes * num_aslots;
 }
 
-int megakernel_variant(int32_t max_k, bool tc) {
-    if (tc) return 2;  // no register-resident matvec input on the batched path
-    const int nch = (max_k / 8 + kComputeThreads - 1) / kComputeThreads;
-    if (nch <= 2) return 2;
-    if (nch <= 4) return 4;
-    if (nch <= 8) return 8;
-    return 16;
+int megakernel_variant(int32_t /*max_k*/, bool /*tc*/) {
+    return 2;  // one build: matvec inputs past 4096 columns stream through L2
 }
 
 cudaError_t megakernel_set_smem(int variant, size_t smem) {

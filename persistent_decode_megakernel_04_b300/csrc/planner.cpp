@@ -61,8 +61,6 @@ mk_status check_cfg(const mk_model_cfg &c) {
     const int32_t group = c.n_q_heads / c.n_kv_heads;
     if (group > 8 || (group & (group - 1)) || c.head_dim > 128) return MK_ERR_UNSUPPORTED;
     if (c.page_size % 64) return MK_ERR_UNSUPPORTED;  // attention reads aligned 64-token blocks of a page
-    // a matvec input is held in registers: at most 16 row pieces of 2048 columns
-    if (std::max({c.hidden, c.ffn_dim, c.n_q_heads * c.head_dim}) > 16 * kMvPiece) return MK_ERR_UNSUPPORTED;
     if (c.batch > kTcMaxBatch) return MK_ERR_UNSUPPORTED;  // one tcgen05 N tile holds the whole batch
     return MK_OK;
 }
@@ -73,7 +71,8 @@ mk_plan_options resolve_options(const mk_model_cfg &cfg, const mk_plan_options *
     if (opt) o = *opt;
     if (o.num_ctas <= 0 || o.num_ctas > num_sms) o.num_ctas = num_sms;
     if (o.slot_bytes <= 0) o.slot_bytes = 32768;
-    if (o.num_slots <= 0) o.num_slots = (cfg.batch > 1) ? 0 : 6;  // batched: as many as shared memory holds
+    const bool tc = cfg.batch > 1 || o.tensor_cores == 1;
+    if (o.num_slots <= 0) o.num_slots = tc ? 0 : 6;  // tensor-core path: as many as shared memory holds
     if (o.timeout_ms <= 0) o.timeout_ms = 2000;
     if (o.attn_splits <= 0) {
         int32_t pairs = cfg.batch * cfg.n_kv_heads;
@@ -103,7 +102,7 @@ mk_status build_plan(const mk_model_cfg &cfg, const mk_plan_options &opt, PlanTa
     mk_status st = check_cfg(cfg);
     if (st != MK_OK) return st;
     const int32_t N = opt.num_ctas;
-    const bool tc = cfg.batch > 1;
+    const bool tc = cfg.batch > 1 || opt.tensor_cores == 1;
     if (N <= 0 || opt.slot_bytes < 4096 || opt.slot_bytes % 1024 || opt.attn_splits <= 0 ||
         opt.attn_splits > kMaxSplits || (tc ? (opt.num_slots == 1 || opt.num_slots < 0) : opt.num_slots < 2))
         return MK_ERR_INVALID;

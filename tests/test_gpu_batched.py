@@ -92,3 +92,12 @@ def test_8b_batched_decode_from_seeded_cache(cuda_device, B):
     model = harness.oracle_model(m)
     caches = harness.fill_synthetic_cache(kv, model, m, ctx, B, max_seq, rows=(0, B - 1))
     harness.run_from_cache(plan, kv, model, caches, ctx, steps, synth.tokens(B, wl.seed, 0, m.vocab), batch=B)
+
+
+def test_tiny_batch1_on_tensor_cores(cuda_device):
+    """Batch 1 with the projections forced onto the tcgen05 path (N padded to
+    16): the same task graph as the batched plans, one live row."""
+    max_seq = 128
+    plan, kv = harness.gpu_plan(TINY, max_seq, batch=1, opts=mk.mk_plan_options(tensor_cores=1))
+    model = harness.oracle_model(TINY)
+    harness.run_teacher_forced_batch(plan, kv, model, prompts(1, 20, seed=5), 5, max_seq)
