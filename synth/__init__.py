@@ -16,6 +16,9 @@ from pathlib import Path
 import numpy as np
 
 from .configs import (  # noqa: F401  (re-exported)
+    TINY_D128,
+    TINY_G8,
+    TINY_MHA,
     LAYER_TIDS,
     TID_EMBED,
     TID_FINAL_NORM,

@@ -51,6 +51,11 @@ class Workload:
 
 
 TINY = ModelCfg("tiny", 2, 256, 4, 2, 64, 688, 1024, rope_theta=1e4)
+# tiny variants covering the other GQA group sizes (8 q heads per kv head as
+# in the 70B shape, and plain multi-head attention) and head_dim 128
+TINY_G8 = ModelCfg("tiny-g8", 2, 256, 16, 2, 64, 688, 1024, rope_theta=1e4)
+TINY_MHA = ModelCfg("tiny-mha", 2, 256, 4, 4, 64, 688, 1024, rope_theta=1e4)
+TINY_D128 = ModelCfg("tiny-d128", 2, 512, 8, 2, 128, 1376, 1024, rope_theta=1e4)
 LLAMA_1B = ModelCfg("llama-3.2-1b-shaped", 16, 2048, 32, 8, 64, 8192, 128256, rope_theta=5e5, tied_embeddings=True)
 LLAMA_8B = ModelCfg("llama-3-8b-shaped", 32, 4096, 32, 8, 128, 14336, 128256, rope_theta=5e5)
 LLAMA_70B = ModelCfg("llama-70b-shaped", 80, 8192, 64, 8, 128, 28672, 128256, rope_theta=5e5)

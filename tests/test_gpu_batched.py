@@ -101,3 +101,59 @@ def test_tiny_batch1_on_tensor_cores(cuda_device):
     plan, kv = harness.gpu_plan(TINY, max_seq, batch=1, opts=mk.mk_plan_options(tensor_cores=1))
     model = harness.oracle_model(TINY)
     harness.run_teacher_forced_batch(plan, kv, model, prompts(1, 20, seed=5), 5, max_seq)
+
+
+@pytest.mark.parametrize("m", [synth.TINY_G8, synth.TINY_MHA, synth.TINY_D128], ids=["g8", "mha", "d128"])
+def test_tiny_variants_batched(cuda_device, m):
+    max_seq = 128
+    plan, kv = harness.gpu_plan(m, max_seq, batch=6)
+    model = harness.oracle_model(m)
+    harness.run_teacher_forced_batch(plan, kv, model, prompts(6, 66, seed=9, vocab=m.vocab), 3, max_seq,
+                                     rows=[0, 5])
+
+
+def test_70b_batched_first_decode_step(cuda_device):
+    """The 70B-shaped decoder on one B300 (141 GB of bf16 weights, batch 16,
+    2048 cached tokens per sequence): the first decode step from a seeded
+    cache, checked by the oracle on rows 0 and 15.  The oracle regenerates
+    each layer's weights on the host and discards them."""
+    import torch
+
+    import oracle
+
+    torch.cuda.empty_cache()
+    wl = WORKLOADS["70b"]
+    m, B, ctx = wl.model, wl.batch, wl.prompt_len
+    max_seq = ((ctx + 1 + 63) // 64) * 64
+    plan, kv = harness.gpu_plan(m, max_seq, batch=B)
+    for l in range(m.n_layers):
+        for which, pool in (("k", kv.k), ("v", kv.v)):
+            synth.device_kv_pages(pool[l], kv.page_table, m, wl.seed, l, which, B, kv.max_pages, ctx, kv.page_size)
+    toks = synth.tokens(B, wl.seed, 0, m.vocab)
+    logits = torch.empty((B, m.vocab), dtype=torch.float32, device=cuda_device)
+    plan.decode_step(torch.tensor(toks, device=cuda_device), torch.full((B,), ctx, dtype=torch.int32,
+                                                                       device=cuda_device), kv, logits)
+    plan.check()
+    got = logits.cpu().numpy()
+    plan.close()
+    del plan, kv
+    torch.cuda.empty_cache()
+
+    emb = synth.normal_bf16((m.vocab, m.hidden), wl.seed, synth.TID_EMBED, m.weight_std)
+    lm = synth.normal_bf16((m.vocab, m.hidden), wl.seed, synth.TID_LM_HEAD, m.weight_std)
+    fin = synth.normal_bf16((m.hidden,), wl.seed, synth.TID_FINAL_NORM, 0.0, 1.0)
+    model = oracle.Model(m, {"embed": emb, "lm_head": lm, "final_norm": fin})
+    rows = (0, B - 1)
+    xs = {b: model.embed_token(int(toks[b])) for b in rows}
+    for l in range(m.n_layers):
+        lw = synth.host_layer_weights(m, wl.seed, l)
+        kh = synth.host_kv(m, wl.seed, l, "k", B, ctx)
+        vh = synth.host_kv(m, wl.seed, l, "v", B, ctx)
+        for b in rows:
+            kc = np.zeros((max_seq, m.n_kv_heads, m.head_dim))
+            vc = np.zeros_like(kc)
+            kc[:ctx] = synth.bf16_to_f64(kh[b])
+            vc[:ctx] = synth.bf16_to_f64(vh[b])
+            model.layer_step(lw, kc, vc, ctx, xs[b])
+    for b in rows:
+        harness.compare_logits(got[b], model.head(xs[b]), f"70B row {b}")

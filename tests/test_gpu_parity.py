@@ -215,3 +215,12 @@ def test_full_size_decode_from_seeded_cache(cuda_device, name, ctx, steps):
     caches = harness.fill_synthetic_cache(kv, model, m, ctx, 1, max_seq)
     stats = harness.run_from_cache(plan, kv, model, caches, ctx, steps, synth.tokens(1, wl.seed, 0, m.vocab))
     print(name, stats)
+
+
+@pytest.mark.parametrize("m", [synth.TINY_G8, synth.TINY_MHA, synth.TINY_D128], ids=["g8", "mha", "d128"])
+def test_tiny_variants_group_sizes_and_head_dim(cuda_device, m):
+    """GQA groups of 8 and 1 (two and one MMA column tiles in attention) and
+    head_dim 128 (two swizzled K/V halves), prompt crossing a KV page."""
+    plan, kv = harness.gpu_plan(m, 128)
+    model = harness.oracle_model(m)
+    harness.run_teacher_forced(plan, kv, model, synth.tokens(70, 0, 8, m.vocab), 4, 128)
