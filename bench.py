@@ -354,6 +354,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prompt-len", type=int, default=0, help="override the workload's prompt length")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (sequences per step)")
+    ap.add_argument("--layers", type=int, default=0, help="profiling only: keep the shape, use this many layers")
     ap.add_argument("--tensor-cores", action="store_true",
                     help="run the projections as tcgen05 tiles at batch 1 too (default: CUDA-core matvecs)")
     ap.add_argument("--trace-out", default="", help="write a per-phase task trace of one extra step here")
@@ -364,6 +365,9 @@ def main():
         wl = replace(wl, prompt_len=args.prompt_len)
     if args.batch > 0:
         wl = replace(wl, batch=args.batch)
+    if args.layers > 0:
+        # profiling a full-width model with fewer layers (the measured workload keeps every layer)
+        wl = replace(wl, model=replace(wl.model, n_layers=args.layers, name=f"{wl.model.name}-{args.layers}l"))
     if args.impl == "reference":
         run_reference(args, wl)
     else:

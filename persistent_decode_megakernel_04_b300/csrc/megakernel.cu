@@ -311,10 +311,43 @@ struct Producer {
         const int op = t.op;
         const MvGeom g = p.mv[op];              // register copies: the copy loop's
         const LayerW lw = p.layers[t.layer];    // inline asm must not force reloads
+        const int32_t qb1 = p.nq * p.d, qb2 = qb1 + p.nkv * p.d, qb3 = p.qkv_rows;
         for (int32_t row = t.a0; row < t.a1;) {
-            const int32_t n = mv_group_rows(p, op, row, t.a1);
+            int32_t n = min(g.rpp, t.a1 - row);
+            if (op == OP_QKV) n = min(n, (row < qb1 ? qb1 : (row < qb2 ? qb2 : qb3)) - row);
             int32_t lr;
             const uint16_t *W = mv_matrix(p, op, lw, row, &lr);
+            if (g.rps == 8 && g.row_mult == 2) {
+                // gate rows and up rows of the group in one slot: two contiguous copies
+                uint32_t s;
+                if (!acquire_slot(c, &s)) return false;
+                const uint32_t bytes = (uint32_t)(n * g.K * 2);
+                mbar_arrive_expect_tx(&c.sc->full[s], 2 * bytes);
+                uint8_t *dst = c.ring + (size_t)s * slot_bytes;
+                bulk_g2s(dst, W + (int64_t)lr * g.K, bytes, &c.sc->full[s], pol);
+                bulk_g2s(dst + (size_t)4 * g.K * 2, lw.w_up + (int64_t)lr * g.K, bytes, &c.sc->full[s], pol);
+                ++issued;
+                row += n;
+                continue;
+            }
+            if (g.rps > 0) {
+                // whole-row slots: rps rows of one matrix, one contiguous copy each
+                for (int m = 0; m < g.row_mult; ++m) {
+                    const uint16_t *Wm = (m == 0) ? W : lw.w_up;
+                    for (int32_t j0 = 0; j0 < n; j0 += g.rps) {
+                        const int32_t cnt = min(g.rps, n - j0);
+                        uint32_t s;
+                        if (!acquire_slot(c, &s)) return false;
+                        const uint32_t bytes = (uint32_t)(cnt * g.K * 2);
+                        mbar_arrive_expect_tx(&c.sc->full[s], bytes);
+                        bulk_g2s(c.ring + (size_t)s * slot_bytes, Wm + (int64_t)(lr + j0) * g.K, bytes, &c.sc->full[s],
+                                 pol);
+                        ++issued;
+                    }
+                }
+                row += n;
+                continue;
+            }
             for (int32_t ks = 0; ks < g.ksplit; ++ks) {
                 uint32_t s;
                 if (!acquire_slot(c, &s)) return false;
@@ -630,15 +663,6 @@ struct Consumer {
     // A failed wait (abort or timeout) marks the CTA aborted but keeps the
     // control flow: all compute warps must reach the same named barriers, so
     // they leave only together, at a task boundary.
-    __device__ uint32_t wait_slot(const Ctx &c) {
-        const uint32_t s = consumed % ns;
-        const uint32_t round = consumed / ns;
-        const uint64_t t0 = tracing ? globaltimer_ns() : 0;
-        wait_mbar(c, &c.sc->full[s], round & 1u, SITE_FULL_WAIT);
-        if (tracing) full_wait_ns += globaltimer_ns() - t0;
-        return s;
-    }
-
     // Wait for ring slot number k (k = consumed + j for lookahead).
     __device__ uint32_t wait_slot_at(const Ctx &c, uint32_t k) {
         const uint32_t s = k % ns;
@@ -647,6 +671,8 @@ struct Consumer {
         if (tracing) full_wait_ns += globaltimer_ns() - t0;
         return s;
     }
+
+    __device__ uint32_t wait_slot(const Ctx &c) { return wait_slot_at(c, consumed); }
 
     // Batch 1: one arrival per compute warp.  Batched path: the slot's empty
     // barrier also takes MMA commits, so it counts one arrival, made after
@@ -707,6 +733,74 @@ struct Consumer {
         for (int r = 0; r < 8; ++r) dot8x2(acc2[r], w[r], xv);
     }
 
+    // Whole-row slot of up to 4 rows of K = KS * 2048 (or fewer) columns:
+    // thread ct loads its chunk of each piece of each row (4 * KS loads),
+    // releases the slot, then accumulates rows into acc[0..3].
+    template <int KS>
+    __device__ __forceinline__ void mv_rows4(const Ctx &c, int32_t nrows, int32_t nch,
+                                             const float (&xr)[kMvResident][8], uint64_t *acc) {
+        const uint32_t s = wait_slot(c);
+        const uint4 *base = reinterpret_cast<const uint4 *>(c.ring + (size_t)s * slot_bytes);
+        uint4 w[4 * KS];
+#pragma unroll
+        for (int q = 0; q < 4 * KS; ++q) {
+            const int r = q / KS, ch = ct + kComputeThreads * (q % KS);
+            w[q] = (r < nrows && ch < nch) ? base[r * nch + ch] : make_uint4(0u, 0u, 0u, 0u);
+        }
+        release_slot(c, s);
+#pragma unroll
+        for (int q = 0; q < 4 * KS; ++q) dot8x2(acc[q / KS], w[q], xr[q % KS]);
+    }
+
+    // Whole-row slot of up to 8 rows of at most 2048 columns.
+    __device__ __forceinline__ void mv_rows8(const Ctx &c, int32_t nrows, int32_t nch, const float (&xv)[8],
+                                             uint64_t (&acc2)[8]) {
+        const uint32_t s = wait_slot(c);
+        const uint4 *base = reinterpret_cast<const uint4 *>(c.ring + (size_t)s * slot_bytes) + ct;
+        uint4 w[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) w[r] = (r < nrows && ct < nch) ? base[r * nch] : make_uint4(0u, 0u, 0u, 0u);
+        release_slot(c, s);
+#pragma unroll
+        for (int r = 0; r < 8; ++r) dot8x2(acc2[r], w[r], xv);
+    }
+
+    // Slot of 4 gate rows then 4 up rows (at most 2048 columns), n of each live.
+    __device__ __forceinline__ void mv_rows8_gu(const Ctx &c, int32_t n, int32_t nch, const float (&xv)[8],
+                                                uint64_t (&acc2)[8]) {
+        const uint32_t s = wait_slot(c);
+        const uint4 *base = reinterpret_cast<const uint4 *>(c.ring + (size_t)s * slot_bytes) + ct;
+        uint4 w[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) w[r] = ((r & 3) < n && ct < nch) ? base[r * nch] : make_uint4(0u, 0u, 0u, 0u);
+        release_slot(c, s);
+#pragma unroll
+        for (int r = 0; r < 8; ++r) dot8x2(acc2[r], w[r], xv);
+    }
+
+    // Both pieces of a two-piece row group at once: 16 loads in flight, then
+    // 16 rows x pieces of paired FMAs (more independent work per warp).
+    __device__ __forceinline__ void mv_group2(const Ctx &c, int32_t pw8a, int32_t pw8b, int32_t R,
+                                              const float (&xa)[8], const float (&xb)[8], uint64_t (&acc2)[8]) {
+        const uint32_t sa = wait_slot(c);
+        const uint4 *ba = reinterpret_cast<const uint4 *>(c.ring + (size_t)sa * slot_bytes) + ct;
+        uint4 wa[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) wa[r] = (ct < pw8a && r < R) ? ba[r * pw8a] : make_uint4(0u, 0u, 0u, 0u);
+        release_slot(c, sa);
+        const uint32_t sb = wait_slot(c);
+        const uint4 *bb = reinterpret_cast<const uint4 *>(c.ring + (size_t)sb * slot_bytes) + ct;
+        uint4 wb[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) wb[r] = (ct < pw8b && r < R) ? bb[r * pw8b] : make_uint4(0u, 0u, 0u, 0u);
+        release_slot(c, sb);
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            dot8x2(acc2[r], wa[r], xa);
+            dot8x2(acc2[r], wb[r], xb);
+        }
+    }
+
     __device__ void run_matvec(const Ctx &c, const Task &t) {
         const KParams &p = *c.p;
         const int op = t.op;
@@ -729,16 +823,16 @@ struct Consumer {
         const float *xin = (op == OP_O) ? p.attn_out : (op == OP_DOWN ? p.hbuf : p.x);
         const uint16_t *gain =
             op == OP_QKV ? lw.attn_norm : (op == OP_GU ? lw.mlp_norm : (op == OP_LM ? p.final_norm : nullptr));
-        const bool resident = g.ksplit <= 2;
-        float xr[2][8];
+        const bool resident = g.ksplit <= kMvResident;
+        float xr[kMvResident][8];
         float ss = 0.f;
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
+        for (int j = 0; j < kMvResident; ++j) {
             load_piece(p, xin, emb_row, nullptr, 1.f, nchunk, j < g.ksplit ? j : 1 << 20, xr[j]);
 #pragma unroll
             for (int e = 0; e < 8; ++e) ss = fmaf(xr[j][e], xr[j][e], ss);
         }
-        for (int j = 2; j < g.ksplit; ++j) {
+        for (int j = kMvResident; j < g.ksplit; ++j) {
             float v[8];
             load_piece(p, xin, emb_row, nullptr, 1.f, nchunk, j, v);
 #pragma unroll
@@ -757,7 +851,7 @@ struct Consumer {
             compute_bar();  // rms_part is reused by the next task
             if (resident) {
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
+                for (int j = 0; j < kMvResident; ++j) {
                     const int32_t ch = ct + kComputeThreads * j;
                     if (ch < nchunk) {
                         const uint4 gv = __ldg(reinterpret_cast<const uint4 *>(gain) + ch);
@@ -769,9 +863,13 @@ struct Consumer {
                 }
             }
         }
-        // streamed inputs: piece ks of the next slot, loaded one slot ahead
-        float xn[8];
-        if (!resident) load_piece(p, xin, emb_row, gain, rn, nchunk, 0, xn);
+        // streamed inputs: the pieces of the next kMvAhead slots, loaded ahead
+        // (a ring of register buffers; slot ks uses buffer ks % kMvAhead)
+        float xq[kMvAhead][8];
+        if (!resident) {
+#pragma unroll
+            for (int a = 0; a < kMvAhead; ++a) load_piece(p, xin, emb_row, gain, rn, nchunk, a % g.ksplit, xq[a]);
+        }
 
         const int lq = lane >> 2;  // row this lane holds after the reduce-scatter
         // group geometry and outputs in registers (the ring's inline asm would
@@ -786,16 +884,38 @@ struct Consumer {
             uint64_t acc2[8];
 #pragma unroll
             for (int r = 0; r < 8; ++r) acc2[r] = 0ull;
-            if (resident) {
+            if (g.rps == 8) {
+                // 8 rows of one matrix, or 4 gate rows (acc 0..3) + 4 up rows (acc 4..7)
+                if (g.row_mult == 2) mv_rows8_gu(c, n, nchunk, xr[0], acc2);
+                else mv_rows8(c, n, nchunk, xr[0], acc2);
+            } else if (g.rps == 4) {
+                // acc rows 0..3: first slot; 4..7: the up rows (gate/up) or rows 4..7
+                const int32_t na = (g.row_mult == 2) ? n : min(n, 4), nb = (g.row_mult == 2) ? n : n - 4;
+                if (g.ksplit == 2) {
+                    mv_rows4<2>(c, na, nchunk, xr, &acc2[0]);
+                    if (nb > 0) mv_rows4<2>(c, nb, nchunk, xr, &acc2[4]);
+                } else {
+                    mv_rows4<1>(c, na, nchunk, xr, &acc2[0]);
+                    if (nb > 0) mv_rows4<1>(c, nb, nchunk, xr, &acc2[4]);
+                }
+            } else if (g.ksplit == 2) {
+                mv_group2(c, g.kc >> 3, (g.K - g.kc) >> 3, R, xr[0], xr[1], acc2);
+            } else if (resident) {
 #pragma unroll
-                for (int ks = 0; ks < 2; ++ks)
+                for (int ks = 0; ks < kMvResident; ++ks)
                     if (ks < g.ksplit) mv_slot(c, min(g.kc, g.K - ks * g.kc) >> 3, R, xr[ks], acc2);
             } else {
                 for (int ks = 0; ks < g.ksplit; ++ks) {
+                    // oldest buffer out, the piece needed kMvAhead slots from now in
+                    // (wrapping into the next group)
                     float xc[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) xc[e] = xn[e];
-                    load_piece(p, xin, emb_row, gain, rn, nchunk, ks + 1 < g.ksplit ? ks + 1 : 0, xn);
+                    for (int e = 0; e < 8; ++e) {
+                        xc[e] = xq[0][e];
+#pragma unroll
+                        for (int a = 0; a + 1 < kMvAhead; ++a) xq[a][e] = xq[a + 1][e];
+                    }
+                    load_piece(p, xin, emb_row, gain, rn, nchunk, (ks + kMvAhead) % g.ksplit, xq[kMvAhead - 1]);
                     mv_slot(c, min(g.kc, g.K - ks * g.kc) >> 3, R, xc, acc2);
                 }
             }
@@ -806,15 +926,19 @@ struct Consumer {
             const float v = warp_reduce8(acc, lane);
             if ((lane & 3) == 0) c.sc->red[red_buf][wc][lq] = v;
             compute_bar();
-            if (ct < n) {
+            // row i of the group is finished by lane 0 of warp i, so no single
+            // warp falls behind the others by the whole group's epilogue
+            if (lane == 0 && wc < n) {
+                const int ri = wc;
                 float tot = 0.f, tot2 = 0.f;
 #pragma unroll
-                for (int w = 0; w < kComputeWarps; ++w) tot += c.sc->red[red_buf][w][ct];
+                for (int w = 0; w < kComputeWarps; ++w) tot += c.sc->red[red_buf][w][ri];
                 if (g.row_mult == 2) {
+                    const int up = (g.rps > 0) ? 4 : n;  // where the group's up rows sit
 #pragma unroll
-                    for (int w = 0; w < kComputeWarps; ++w) tot2 += c.sc->red[red_buf][w][n + ct];
+                    for (int w = 0; w < kComputeWarps; ++w) tot2 += c.sc->red[red_buf][w][up + ri];
                 }
-                const int32_t orow = row + ct;
+                const int32_t orow = row + ri;
                 float xo = 0.f;
                 if (has_resid) {
                     xo = resid_in_smem ? c.sc->resid[orow - t.a0]

@@ -21,6 +21,8 @@ constexpr int kAttnBlock = 64;    // cached tokens per attention block (one alig
 constexpr int kQhlStride = kMaxHeadDim + 8;  // bf16 row stride of the split queries (conflict-free ldmatrix)
 constexpr int kPhlStride = kAttnBlock + 8;   // bf16 row stride of the split softmax weights
 constexpr int kMaxResid = 512;    // residual rows prefetched per matvec task
+constexpr int kMvResident = 2;    // matvec inputs of up to 2 x 2048 columns stay in registers
+constexpr int kMvAhead = 3;       // longer inputs: pieces loaded this many slots ahead
 constexpr int kMaxASlots = 8;     // activation ring slots (batched path)
 
 struct KParams {

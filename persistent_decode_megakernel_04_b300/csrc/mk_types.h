@@ -38,17 +38,22 @@ struct LayerW {
     const uint16_t *attn_norm, *wq, *wk, *wv, *wo, *mlp_norm, *w_gate, *w_up, *w_down;
 };
 
-// How a matvec operator's weight rows are cut into ring slots: a row is cut
-// into `ksplit` pieces of `kc` columns (the last may be shorter), and a slot
-// holds piece ks of `rpp` consecutive rows (times 2 for gate/up, which
-// streams matching gate and up rows).
+// How a matvec operator's weight rows are cut into ring slots.  A row is
+// cut into `ksplit` pieces of `kc` columns (the last may be shorter); each
+// compute thread owns column chunk ct of every piece.  Rows are processed in
+// groups of `rpp` (gate/up: rpp gate rows and the matching up rows).
+//  - Whole-row slots (rps > 0, inputs of at most 4096 columns): a slot holds
+//    rps consecutive whole rows of one matrix, one contiguous copy.
+//  - Piece slots (rps == 0): a slot holds piece ks of the group's rows
+//    (gate rows, then up rows).
 struct MvGeom {
     int32_t K;        // input length (columns)
     int32_t rows;     // output rows of the operator
-    int32_t rpp;      // rows per slot
+    int32_t rpp;      // rows per group (of each matrix, for gate/up)
     int32_t ksplit;   // column pieces per row
     int32_t kc;       // columns per piece (2048, or K when K is shorter)
     int32_t row_mult; // 2 for gate/up, else 1
+    int32_t rps;      // whole-row slots: rows of one matrix per slot (4 or 8); 0: piece slots
 };
 
 // Batched path: an operator's weight [rows x K] is cut into units of

@@ -43,7 +43,16 @@ MvGeom make_geom(int32_t K, int32_t rows, int32_t row_mult, int32_t slot_bytes) 
     g.row_mult = row_mult;
     g.kc = std::min(K, kMvPiece);
     g.ksplit = (K + g.kc - 1) / g.kc;
-    g.rpp = std::min(8 / row_mult, slot_bytes / (row_mult * g.kc * 2));
+    if (g.ksplit <= 2 && slot_bytes >= 4 * K * 2) {
+        // whole-row slots: one contiguous copy per slot, 4 (or 8 short) rows of one matrix
+        // (gate/up at most 2048 columns: 4 gate rows and the matching 4 up rows
+        // share a slot, as two contiguous copies; rps = 8 then counts both)
+        g.rpp = 8 / row_mult;
+        g.rps = (g.ksplit == 1 && slot_bytes >= 8 * K * 2) ? 8 : 4;
+    } else {
+        g.rpp = std::min(8 / row_mult, slot_bytes / (row_mult * g.kc * 2));
+        g.rps = 0;
+    }
     return g;
 }
 
