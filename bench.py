@@ -55,6 +55,38 @@ def step_bytes(m, batch: int, ctx: int) -> int:
     return weight_bytes_read(m, batch) + batch * (per_tok * (ctx - 1) + per_tok + m.vocab * 4)
 
 
+# DRAM bytes (read + write) of one megakernel launch from an ncu capture of
+# the full-size workload (dram__bytes_read.sum + dram__bytes_write.sum, one
+# pass), keyed by (workload, batch) and by the fingerprint of the kernel
+# sources the capture ran.  A source change makes the entry stale and the
+# bench line reports null.
+NCU_TRAFFIC = {
+    ("8b", 1): {"fingerprint": "f4d3ed062725e6ee", "bytes": 15.02e9 + 57.2e6,
+                "summary": "profiles/megakernel_8b_b1_dram.md"},
+}
+
+
+def kernel_fingerprint() -> str:
+    """sha256 (first 16 hex digits) over the kernel sources, file by file."""
+    import hashlib
+    h = hashlib.sha256()
+    root = ROOT / "persistent_decode_megakernel_04_b300" / "csrc"
+    for p in sorted(root.iterdir()):
+        if p.suffix in (".cu", ".cuh", ".h", ".cpp"):
+            h.update(p.name.encode())
+            h.update(p.read_bytes())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str, batch: int, overridden: int):
+    """Bytes per launch of the capture above, or None when the workload was
+    cut or resized or the kernel sources changed since."""
+    e = NCU_TRAFFIC.get((workload, batch))
+    if e is None or overridden or e["fingerprint"] != kernel_fingerprint():
+        return None
+    return e["bytes"]
+
+
 def measured_peak():
     p = ROOT / "MEASURED_PEAKS.json"
     if p.exists():
@@ -321,11 +353,12 @@ def run_mk(args, wl):
                        "projections": "tcgen05 tiles" if (B > 1 or args.tensor_cores) else "CUDA-core matvec",
                        "ctx_first_timed": ctx0, "ctx_last_timed": ctx0 + args.steps - 1,
                        "parallelism": f"replicas x{world}",
-                       "l2": "no flush: ~15 GB of weights stream per step (> 126 MB L2)"},
+                       "l2": f"no flush: {weight_bytes_read(m, B) / 1e9:.1f} GB of weights stream per step (> 126 MB L2)"},
             "tokens_per_s": 1e3 / ms_step * B * world,
             "hbm_gbs": achieved,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "peak_source": peak_src, "traffic": None,
+                         "frac": achieved / peak, "peak_source": peak_src,
+                         "traffic": ncu_traffic(args.workload, B, args.layers or args.prompt_len),
                          "kernel": "megakernel", "kernel_ms_mean": statistics.mean(kern_ms),
                          "bytes_per_step_mean": bytes_total / args.steps},
             "clocks": clk,
