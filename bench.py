@@ -222,7 +222,11 @@ def run_mk(args, wl):
     B = wl.batch
     max_seq = ((wl.prompt_len + args.warmup + args.steps + args.e2e_steps + 4 + 63) // 64) * 64
     weights = synth.device_weights(m, wl.seed, device=dev)
-    popts = mk.mk_plan_options(tensor_cores=1) if args.tensor_cores else None
+    kw = dict(kv.split("=") for kv in args.plan_opt)
+    kw = {k: int(v) for k, v in kw.items()}
+    if args.tensor_cores:
+        kw["tensor_cores"] = 1
+    popts = mk.mk_plan_options(**kw) if kw else None
     plan = mk.Plan(m, weights, batch=B, max_seq=max_seq, opts=popts)
     kv = mk.KVCache(m, B, max_seq, shuffle_seed=1, device=dev)
     logits = torch.empty((B, m.vocab), dtype=torch.float32, device=dev)
@@ -324,7 +328,7 @@ def run_mk(args, wl):
         # one more step with a tracing plan over the same weights and cache
         from persistent_decode_megakernel_04_b300 import trace as mktrace
 
-        topt = mk.mk_plan_options(trace=1, tensor_cores=1 if args.tensor_cores else 0)
+        topt = mk.mk_plan_options(**{**kw, "trace": 1})
         tplan = mk.Plan(m, weights, batch=B, max_seq=max_seq, opts=topt)
         tpos = h_pos.to(dev)
         for _ in range(2):
@@ -353,6 +357,7 @@ def run_mk(args, wl):
                        "projections": "tcgen05 tiles" if (B > 1 or args.tensor_cores) else "CUDA-core matvec",
                        "ctx_first_timed": ctx0, "ctx_last_timed": ctx0 + args.steps - 1,
                        "parallelism": f"replicas x{world}",
+                       **({"plan_options": kw} if kw else {}),
                        "l2": f"no flush: {weight_bytes_read(m, B) / 1e9:.1f} GB of weights stream per step (> 126 MB L2)"},
             "tokens_per_s": 1e3 / ms_step * B * world,
             "hbm_gbs": achieved,
@@ -390,6 +395,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="profiling only: keep the shape, use this many layers")
     ap.add_argument("--tensor-cores", action="store_true",
                     help="run the projections as tcgen05 tiles at batch 1 too (default: CUDA-core matvecs)")
+    ap.add_argument("--plan-opt", action="append", default=[], metavar="FIELD=INT",
+                    help="set an mk_plan_options field (tuning sweeps), e.g. max_inflight=3")
     ap.add_argument("--trace-out", default="", help="write a per-phase task trace of one extra step here")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

@@ -112,7 +112,9 @@ typedef struct {
     int32_t trace;         /* nonzero: record per-task timestamps (see mk_plan_trace) */
     int32_t tensor_cores;  /* 0: projections as CUDA-core matvecs at batch 1, tcgen05 tiles at
                               batch >= 2; 1: tcgen05 tiles at every batch */
-    int32_t reserved[6];
+    int32_t max_inflight;  /* ring copies a CTA keeps in flight at once (default: 2 at batch 1,
+                              every free ring slot when batched; >= num_slots: no cap) */
+    int32_t reserved[5];
 } mk_plan_options;
 
 typedef struct mk_plan mk_plan; /* opaque, library-owned */

@@ -45,6 +45,19 @@ namespace mk {
 
 namespace {
 
+// Attention scratch of one task; the batch-1 matvec reuses the same bytes
+// for its per-warp row totals (a CTA runs one task at a time).
+struct AttnScratch {
+    alignas(16) float q_s[kMaxGroup][kMaxHeadDim];        // RoPE'd, scaled queries (fp32)
+    alignas(16) float s_s[kMaxGroup][kAttnBlock];         // scores of one 64-token block
+    alignas(16) uint16_t q_hl[2 * kMaxGroup][kQhlStride];  // queries as bf16 high parts, then low parts
+    alignas(16) uint16_t p_hl[2 * kMaxGroup][kPhlStride];  // softmax weights, bf16 high then low parts
+};
+
+// Row groups (of at most 8 output values) whose per-warp totals a batch-1
+// matvec task keeps in shared memory before one barrier finishes them.
+constexpr int kPartGroups = 48;
+
 struct SmemCtl {
     uint64_t full[kMaxSlots];
     uint64_t empty[kMaxSlots];
@@ -52,16 +65,18 @@ struct SmemCtl {
     uint32_t abort;      // local abort flag
     uint32_t last_flag;  // attention: this CTA finished the last split of a head
     uint32_t pad0;
-    float red[2][kComputeWarps][8];
     float rms_part[kComputeWarps];
     float att_m[kMaxGroup], att_l[kMaxGroup], att_alpha[kMaxGroup];
     float att_inv_l[kMaxGroup];
-    float merge_w[kMaxSplits][kMaxGroup];  // split weights exp(m_s - max_s m_s) of the merge
+    float merge_w[kMaxSplits][kMaxGroup];  // live split j's weight exp(m_j - max m) in the merge
+    float merge_l[kMaxSplits][kMaxGroup];  // live split j's sum of exponentials
     float resid[kMaxResid];                // residual rows of an O / down task, read at task start
-    alignas(16) float q_s[kMaxGroup][kMaxHeadDim];        // RoPE'd, scaled queries (fp32)
-    alignas(16) float s_s[kMaxGroup][kAttnBlock];         // scores of one 64-token block
-    alignas(16) uint16_t q_hl[2 * kMaxGroup][kQhlStride];  // queries as bf16 high parts, then low parts
-    alignas(16) uint16_t p_hl[2 * kMaxGroup][kPhlStride];  // softmax weights, bf16 high then low parts
+    union {
+        AttnScratch at;
+        alignas(16) float mv_part[kPartGroups][8][kComputeWarps];  // [group][value][warp]
+    };
+    int32_t mv_grow[kPartGroups];  // first output row of each waiting group
+    int32_t mv_gn[kPartGroups];    // rows in it
     float att_pnew[kMaxGroup];                             // weight of the new token
     alignas(16) uint16_t knew[kMaxHeadDim];
     alignas(16) uint16_t vnew[kMaxHeadDim];
@@ -76,6 +91,9 @@ struct SmemCtl {
     float rs[kTcMaxBatch];        // 1/rms of each sequence's projection input
     float ssq_red[4][kTcMaxBatch];  // per-epilogue-warp partial sums of x^2
 };
+
+static_assert(sizeof(float) * kPartGroups * 8 * kComputeWarps <= sizeof(AttnScratch),
+              "the matvec row totals must fit in the attention scratch they share");
 
 // The rings start at the first 1024-byte boundary after the control block
 // (the 128-byte-swizzled TMA tiles of the batched path need that alignment);
@@ -226,17 +244,6 @@ __device__ bool wait_mbar(const Ctx &c, uint64_t *bar, uint32_t parity, int32_t 
 // A task's immutable operands are cut into ring-slot "pages"; producer and
 // consumers enumerate them with the same loops.
 
-__device__ __forceinline__ int32_t qkv_boundary(const KParams &p, int32_t row) {
-    const int32_t qr = p.nq * p.d, kr = qr + p.nkv * p.d;
-    return row < qr ? qr : (row < kr ? kr : p.qkv_rows);
-}
-
-__device__ __forceinline__ int32_t mv_group_rows(const KParams &p, int op, int32_t row, int32_t row_end) {
-    int32_t n = min(p.mv[op].rpp, row_end - row);
-    if (op == OP_QKV) n = min(n, qkv_boundary(p, row) - row);
-    return n;
-}
-
 // matrix and local row of operator row `row` (w: the layer's pointers, held
 // in registers by the caller)
 __device__ __forceinline__ const uint16_t *mv_matrix(const KParams &p, int op, const LayerW &w, int32_t row,
@@ -264,6 +271,7 @@ struct AttnRange {
     int32_t pos;       // position of the new token
     int32_t blo, bhi;  // 64-token blocks [blo, bhi) of the cached context [0, pos)
     bool has_new;      // this split also attends to the new token
+    int32_t n_live;    // splits of this (sequence, kv head) with any work
 };
 
 // The cached context [0, pos) is cut into aligned 64-token blocks, and split
@@ -276,7 +284,20 @@ __device__ __forceinline__ AttnRange attn_range(const KParams &p, const Task &t)
     r.blo = (int32_t)((int64_t)t.a2 * nb / t.a3);
     r.bhi = (int32_t)((int64_t)(t.a2 + 1) * nb / t.a3);
     r.has_new = (t.a2 == t.a3 - 1);
+    // nb <= S blocks land on nb distinct splits (the last one among them);
+    // with no cached block only the new token's split works
+    r.n_live = nb < 1 ? 1 : (nb < t.a3 ? (int32_t)nb : t.a3);
     return r;
+}
+
+// The j-th of the r.n_live splits with work (cached blocks, or the new
+// token: the last split).  With nb <= S blocks, block j is the only block of
+// split ((j + 1) S - 1) / nb; with more blocks every split has some.
+__device__ __forceinline__ int32_t live_split(int32_t pos, int32_t j, int32_t S) {
+    const int64_t nb = (pos + kAttnBlock - 1) / kAttnBlock;
+    if (nb == 0) return S - 1;
+    if (nb > S) return j;
+    return (int32_t)(((int64_t)(j + 1) * S - 1) / nb);
 }
 
 __device__ __forceinline__ int64_t kv_offset(const KParams &p, int layer, int32_t page, int32_t kvh, int32_t slot) {
@@ -291,12 +312,21 @@ struct Producer {
     uint64_t *tr = nullptr;  // trace entry of the current task
     uint32_t ns = 0;         // ring slots (kept in a register)
     uint32_t slot_bytes = 0;
+    uint32_t fmax = 0;       // copies in flight at most (0: every free slot)
 
     __device__ bool acquire_slot(const Ctx &c, uint32_t *slot) {
         const uint32_t s = issued % ns;
         const uint32_t round = issued / ns;
         const uint64_t t0 = tr ? globaltimer_ns() : 0;
         if (!wait_mbar(c, &c.sc->empty[s], (round & 1u) ^ 1u, SITE_EMPTY_WAIT)) return false;
+        if (fmax != 0 && issued >= fmax) {
+            // copy number issued - fmax must have landed: fewer bytes queued
+            // in the memory system ahead of this SM's other requests, and a
+            // gpu-scope fence (which waits for this SM's copies in flight)
+            // stays short
+            const uint32_t k = issued - fmax;
+            if (!wait_mbar(c, &c.sc->full[k % ns], (k / ns) & 1u, SITE_EMPTY_WAIT)) return false;
+        }
         if (tr) {
             const uint64_t t1 = globaltimer_ns();
             if (tr[4] == 0) tr[4] = t1;
@@ -449,6 +479,7 @@ __device__ void producer_role(const Ctx &c, const Task *q, int nt) {
     pr.pol = policy_evict_first();
     pr.ns = (uint32_t)c.p->num_slots;
     pr.slot_bytes = (uint32_t)c.p->slot_bytes;
+    pr.fmax = (c.p->max_inflight > 0 && (uint32_t)c.p->max_inflight < pr.ns) ? (uint32_t)c.p->max_inflight : 0u;
     for (int i = 0; i < nt; ++i) {
         const Task t = q[i];
         if (!task_active(*c.p, t)) continue;
@@ -515,7 +546,8 @@ __device__ void scheduler_loop(const Ctx &c, const Task *q, int nt, ActProducer 
                 const uint64_t t0 = globaltimer_ns();
                 uint64_t next = t0 + kAbortCheckNs;
                 for (;;) {
-                    if (ld_acquire_gpu(ctr) >= t.wait_count) break;
+                    // relaxed polls; one acquire once the count is seen
+                    if (ld_relaxed_gpu(ctr) >= t.wait_count && ld_acquire_gpu(ctr) >= t.wait_count) break;
                     const uint64_t now = globaltimer_ns();
                     if (now >= next) {
                         if (local_abort(c) || global_abort(p)) {
@@ -634,18 +666,6 @@ __device__ __forceinline__ float sum_x2(uint64_t acc) {
     return __uint_as_float((uint32_t)acc) + __uint_as_float((uint32_t)(acc >> 32));
 }
 
-__device__ __forceinline__ float dot8(const uint4 w, const float *x) {
-    float a = bf16_lo(w.x) * x[0];
-    a = fmaf(bf16_hi(w.x), x[1], a);
-    a = fmaf(bf16_lo(w.y), x[2], a);
-    a = fmaf(bf16_hi(w.y), x[3], a);
-    a = fmaf(bf16_lo(w.z), x[4], a);
-    a = fmaf(bf16_hi(w.z), x[5], a);
-    a = fmaf(bf16_lo(w.w), x[6], a);
-    a = fmaf(bf16_hi(w.w), x[7], a);
-    return a;
-}
-
 struct Consumer {
     uint32_t ns = 0;         // ring slots and slot size (kept in registers)
     uint32_t slot_bytes = 0;
@@ -654,7 +674,6 @@ struct Consumer {
     uint32_t aconsumed = 0;  // activation ring slots (batched path)
     uint32_t seg = 0;        // accumulator segments (batched path)
     int ct, wc, lane;  // compute-thread index, compute-warp index, lane
-    uint32_t red_buf = 0;
     bool tracing = false;
     uint64_t full_wait_ns = 0;  // traced: waits for filled weight / KV slots
     uint64_t act_wait_ns = 0;   // traced (batched): waits for activation tiles
@@ -877,6 +896,7 @@ struct Consumer {
         const int32_t qb1 = p.nq * p.d, qb2 = qb1 + p.nkv * p.d, qb3 = p.qkv_rows;
         float *const out_qkv = p.qkv, *const out_x = p.x, *const out_h = p.hbuf, *const out_logits = p.logits;
         const uint16_t *const embed_row = p.embed + (int64_t)token * p.H;
+        int32_t pg = 0;  // row groups waiting in mv_part
         for (int32_t row = t.a0; row < t.a1;) {
             int32_t n = min(g.rpp, t.a1 - row);
             if (op == OP_QKV) n = min(n, (row < qb1 ? qb1 : (row < qb2 ? qb2 : qb3)) - row);
@@ -919,43 +939,65 @@ struct Consumer {
                     mv_slot(c, min(g.kc, g.K - ks * g.kc) >> 3, R, xc, acc2);
                 }
             }
-            // reduce-scatter of the 8 row sums over the warp: lane l ends with row l/4
+            // reduce-scatter of the 8 row sums over the warp: lane l ends with
+            // value l/4; this warp's totals wait in shared memory, so the warps
+            // never meet per group (they drift apart by up to the ring's depth)
             float acc[8];
 #pragma unroll
             for (int r = 0; r < 8; ++r) acc[r] = sum_x2(acc2[r]);
             const float v = warp_reduce8(acc, lane);
-            if ((lane & 3) == 0) c.sc->red[red_buf][wc][lq] = v;
-            compute_bar();
-            // row i of the group is finished by lane 0 of warp i, so no single
-            // warp falls behind the others by the whole group's epilogue
-            if (lane == 0 && wc < n) {
-                const int ri = wc;
-                float tot = 0.f, tot2 = 0.f;
-#pragma unroll
-                for (int w = 0; w < kComputeWarps; ++w) tot += c.sc->red[red_buf][w][ri];
-                if (g.row_mult == 2) {
-                    const int up = (g.rps > 0) ? 4 : n;  // where the group's up rows sit
-#pragma unroll
-                    for (int w = 0; w < kComputeWarps; ++w) tot2 += c.sc->red[red_buf][w][up + ri];
-                }
-                const int32_t orow = row + ri;
-                float xo = 0.f;
-                if (has_resid) {
-                    xo = resid_in_smem ? c.sc->resid[orow - t.a0]
-                                       : ((op == OP_O && t.layer == 0)
-                                              ? __uint_as_float((uint32_t)embed_row[orow] << 16)
-                                              : __ldcg(out_x + orow));
-                }
-                switch (op) {
-                    case OP_QKV: out_qkv[orow] = tot; break;
-                    case OP_O:
-                    case OP_DOWN: out_x[orow] = xo + tot; break;
-                    case OP_GU: out_h[orow] = tot / (1.f + expf(-tot)) * tot2; break;
-                    default: out_logits[orow] = tot; break;
-                }
+            if ((lane & 3) == 0) c.sc->mv_part[pg][lq][wc] = v;
+            if (ct == 0) {
+                c.sc->mv_grow[pg] = row;
+                c.sc->mv_gn[pg] = n;
             }
-            red_buf ^= 1u;
+            ++pg;
             row += n;
+            if (pg == kPartGroups || row >= t.a1) {
+                compute_bar();  // every warp's totals of the waiting groups are in
+                mv_finish(c, t, g, pg, resid_in_smem, out_qkv, out_x, out_h, out_logits, embed_row);
+                pg = 0;
+                if (row < t.a1) compute_bar();  // the buffer is refilled
+            }
+        }
+    }
+
+    // Output rows of the pg waiting groups, one (group, row) per thread: the
+    // sum over the warps' totals and the fused epilogue (residual add,
+    // SiLU(gate) * up, or the raw value).
+    __device__ __forceinline__ void mv_finish(const Ctx &c, const Task &t, const MvGeom &g, int32_t pg,
+                                              bool resid_in_smem, float *out_qkv, float *out_x, float *out_h,
+                                              float *out_logits, const uint16_t *embed_row) const {
+        const int op = t.op;
+        for (int32_t i = ct; i < pg * 8; i += kComputeThreads) {
+            const int32_t gi = i >> 3, ri = i & 7;
+            const int32_t n = c.sc->mv_gn[gi];
+            if (ri >= n) continue;
+            const float4 *pv = reinterpret_cast<const float4 *>(&c.sc->mv_part[gi][ri][0]);
+            const float4 a = pv[0], b = pv[1];
+            const float tot = ((a.x + a.y) + (a.z + a.w)) + ((b.x + b.y) + (b.z + b.w));
+            const int32_t orow = c.sc->mv_grow[gi] + ri;
+            switch (op) {
+                case OP_QKV: out_qkv[orow] = tot; break;
+                case OP_GU: {
+                    const int up = (g.rps > 0) ? 4 : n;  // where the group's up rows sit
+                    const float4 *pu = reinterpret_cast<const float4 *>(&c.sc->mv_part[gi][up + ri][0]);
+                    const float4 ua = pu[0], ub = pu[1];
+                    const float tot2 = ((ua.x + ua.y) + (ua.z + ua.w)) + ((ub.x + ub.y) + (ub.z + ub.w));
+                    out_h[orow] = tot / (1.f + expf(-tot)) * tot2;
+                    break;
+                }
+                case OP_O:
+                case OP_DOWN: {
+                    const float xo = resid_in_smem ? c.sc->resid[orow - t.a0]
+                                                   : ((op == OP_O && t.layer == 0)
+                                                          ? __uint_as_float((uint32_t)embed_row[orow] << 16)
+                                                          : __ldcg(out_x + orow));
+                    out_x[orow] = xo + tot;
+                    break;
+                }
+                default: out_logits[orow] = tot; break;
+            }
         }
     }
 
@@ -1071,7 +1113,7 @@ struct Consumer {
 #pragma unroll
                         for (int i = 0; i < 16; ++i) __stcg(mine + ((size_t)m * p.npad + c0 + i) * kTcTileM + r, v[i]);
                     }
-                __threadfence();
+                // the barrier, then one acq_rel atomic (cumulative release) publishes every thread's partial
                 epi_bar();
                 if (et == 0) {
                     uint32_t n_contrib = 0;  // non-empty ranges meeting this tile
@@ -1252,52 +1294,81 @@ struct Consumer {
         const int G = p.nq / p.nkv, NT = (2 * G + 7) / 8;
         const int b = t.a0, kvh = t.a1, S = t.a3;
         const AttnRange r = attn_range(p, t);
+        // a split with no cached block and without the new token neither
+        // computes nor takes part in the merge (short contexts leave most
+        // splits empty)
+        if (r.blo == r.bhi && !r.has_new) return;
         const float *qkv = p.qkv + (int64_t)b * p.qkv_rows;
         const float2 *rope = p.rope + (int64_t)r.pos * half;
         const float scale = rsqrtf((float)d);
         const int ts = p.attn_ts, nsl = kAttnBlock / ts, ts_log2 = (ts == 64) ? 6 : 5;
 
+        // Every load of the setup (queries, RoPE factors, the new token's k
+        // and v, its page) is issued before any is used: one round trip.
+        // Thread ct: query pairs (idx, idx + d/2) for idx = ct, ct + 256
+        // (G d/2 <= 512), the k pair (ct, ct + d/2), v element ct (d <= 128).
+        const float *kh = qkv + (int64_t)p.nq * d + (int64_t)kvh * d;
+        const float *vh = qkv + (int64_t)(p.nq + p.nkv) * d + (int64_t)kvh * d;
+        float qa[2] = {0.f, 0.f}, qb2[2] = {0.f, 0.f}, ka = 0.f, kb = 0.f, vv = 0.f;
+        float2 qcs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)}, kcs = make_float2(0.f, 0.f);
+        int32_t new_page = 0;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int idx = ct + kComputeThreads * k;
+            if (idx < G * half) {
+                const float *qh = qkv + (int64_t)(kvh * G + idx / half) * d + idx % half;
+                qa[k] = __ldcg(qh);
+                qb2[k] = __ldcg(qh + half);
+                qcs[k] = rope[idx % half];
+            }
+        }
+        if (r.has_new) {
+            if (ct < half) {
+                ka = __ldcg(kh + ct);
+                kb = __ldcg(kh + ct + half);
+                kcs = rope[ct];
+            }
+            if (ct < d) vv = __ldcg(vh + ct);
+            new_page = p.page_table[(int64_t)b * p.max_pages + r.pos / p.page_size];
+        }
         // RoPE'd, pre-scaled queries of the G heads sharing this kv head, in
         // fp32 and split into bf16 high / low parts (rows G..2G-1 the low parts)
-        for (int idx = ct; idx < G * half; idx += kComputeThreads) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int idx = ct + kComputeThreads * k;
+            if (idx >= G * half) continue;
             const int g = idx / half, i = idx % half;
-            const float *qh = qkv + (int64_t)(kvh * G + g) * d;
-            const float a = __ldcg(qh + i), bb = __ldcg(qh + i + half);
-            const float2 cs = rope[i];
+            const float a = qa[k], bb = qb2[k];
+            const float2 cs = qcs[k];
             const float q0 = (a * cs.x - bb * cs.y) * scale, q1 = (a * cs.y + bb * cs.x) * scale;
-            sc->q_s[g][i] = q0;
-            sc->q_s[g][i + half] = q1;
+            sc->at.q_s[g][i] = q0;
+            sc->at.q_s[g][i + half] = q1;
             const uint16_t h0 = f32_to_bf16_bits(q0), h1 = f32_to_bf16_bits(q1);
-            sc->q_hl[g][i] = h0;
-            sc->q_hl[g][i + half] = h1;
-            sc->q_hl[G + g][i] = f32_to_bf16_bits(q0 - __uint_as_float((uint32_t)h0 << 16));
-            sc->q_hl[G + g][i + half] = f32_to_bf16_bits(q1 - __uint_as_float((uint32_t)h1 << 16));
+            sc->at.q_hl[g][i] = h0;
+            sc->at.q_hl[g][i + half] = h1;
+            sc->at.q_hl[G + g][i] = f32_to_bf16_bits(q0 - __uint_as_float((uint32_t)h0 << 16));
+            sc->at.q_hl[G + g][i + half] = f32_to_bf16_bits(q1 - __uint_as_float((uint32_t)h1 << 16));
         }
         // MMA columns past 2G stay zero
         for (int idx = ct; idx < (8 * NT - 2 * G) * kQhlStride; idx += kComputeThreads)
-            sc->q_hl[2 * G + idx / kQhlStride][idx % kQhlStride] = 0;
+            sc->at.q_hl[2 * G + idx / kQhlStride][idx % kQhlStride] = 0;
         for (int idx = ct; idx < (8 * NT - 2 * G) * kPhlStride; idx += kComputeThreads)
-            sc->p_hl[2 * G + idx / kPhlStride][idx % kPhlStride] = 0;
+            sc->at.p_hl[2 * G + idx / kPhlStride][idx % kPhlStride] = 0;
         if (r.has_new) {
             // K/V of the new token: RoPE on k, round to bf16, append to the cache
-            const float *kh = qkv + (int64_t)p.nq * d + (int64_t)kvh * d;
-            const float *vh = qkv + (int64_t)(p.nq + p.nkv) * d + (int64_t)kvh * d;
-            const int32_t pg = p.page_table[(int64_t)b * p.max_pages + r.pos / p.page_size];
-            const int64_t off = kv_offset(p, t.layer, pg, kvh, r.pos % p.page_size);
-            for (int i = ct; i < half; i += kComputeThreads) {
-                const float a = __ldcg(kh + i), bb = __ldcg(kh + i + half);
-                const float2 cs = rope[i];
-                const uint16_t k0 = f32_to_bf16_bits(a * cs.x - bb * cs.y);
-                const uint16_t k1 = f32_to_bf16_bits(a * cs.y + bb * cs.x);
-                sc->knew[i] = k0;
-                sc->knew[i + half] = k1;
-                p.k_pool[off + i] = k0;
-                p.k_pool[off + i + half] = k1;
+            const int64_t off = kv_offset(p, t.layer, new_page, kvh, r.pos % p.page_size);
+            if (ct < half) {
+                const uint16_t k0 = f32_to_bf16_bits(ka * kcs.x - kb * kcs.y);
+                const uint16_t k1 = f32_to_bf16_bits(ka * kcs.y + kb * kcs.x);
+                sc->knew[ct] = k0;
+                sc->knew[ct + half] = k1;
+                p.k_pool[off + ct] = k0;
+                p.k_pool[off + ct + half] = k1;
             }
-            for (int i = ct; i < d; i += kComputeThreads) {
-                const uint16_t v = f32_to_bf16_bits(__ldcg(vh + i));
-                sc->vnew[i] = v;
-                p.v_pool[off + i] = v;
+            if (ct < d) {
+                const uint16_t v = f32_to_bf16_bits(vv);
+                sc->vnew[ct] = v;
+                p.v_pool[off + ct] = v;
             }
         }
         if (ct < G) {
@@ -1306,7 +1377,7 @@ struct Consumer {
         }
         compute_bar();
 
-        const uint32_t qb = smem_u32(&sc->q_hl[0][0]);  // B operand (Q^T) of the score MMAs
+        const uint32_t qb = smem_u32(&sc->at.q_hl[0][0]);  // B operand (Q^T) of the score MMAs
         // hi/lo column pairing of the MMA C fragment: column n holds the high
         // part of head n (n < G) or the low part of head n - G
         const int tr = lane >> 2, cq = lane & 3;
@@ -1349,7 +1420,7 @@ struct Consumer {
                     const int tok = 16 * wc + tr + (i >> 1) * 8;
                     const int head = (G == 1) ? 0 : 2 * cq + (i & 1);
                     const bool live = head_lane && (G != 1 || (i & 1) == 0);
-                    if (live) sc->s_s[head][tok] = (tok0 + tok < r.pos) ? v : -INFINITY;
+                    if (live) sc->at.s_s[head][tok] = (tok0 + tok < r.pos) ? v : -INFINITY;
                 }
             }
             compute_bar();
@@ -1357,17 +1428,17 @@ struct Consumer {
             // online softmax, warp g for head g: weights as bf16 high / low parts
             if (wc < G) {
                 const int g = wc;
-                const float s0 = sc->s_s[g][lane], s1 = sc->s_s[g][lane + 32];
+                const float s0 = sc->at.s_s[g][lane], s1 = sc->at.s_s[g][lane + 32];
                 const float m_old = sc->att_m[g];
                 const float m_new = fmaxf(m_old, warp_max(fmaxf(s0, s1)));
                 const float p0 = (s0 == -INFINITY) ? 0.f : expf(s0 - m_new);
                 const float p1 = (s1 == -INFINITY) ? 0.f : expf(s1 - m_new);
                 const float sum = warp_sum(p0 + p1);
                 const uint16_t h0 = f32_to_bf16_bits(p0), h1 = f32_to_bf16_bits(p1);
-                sc->p_hl[g][lane] = h0;
-                sc->p_hl[g][lane + 32] = h1;
-                sc->p_hl[G + g][lane] = f32_to_bf16_bits(p0 - __uint_as_float((uint32_t)h0 << 16));
-                sc->p_hl[G + g][lane + 32] = f32_to_bf16_bits(p1 - __uint_as_float((uint32_t)h1 << 16));
+                sc->at.p_hl[g][lane] = h0;
+                sc->at.p_hl[g][lane + 32] = h1;
+                sc->at.p_hl[G + g][lane] = f32_to_bf16_bits(p0 - __uint_as_float((uint32_t)h0 << 16));
+                sc->at.p_hl[G + g][lane + 32] = f32_to_bf16_bits(p1 - __uint_as_float((uint32_t)h1 << 16));
                 if (lane == 0) {
                     const float alpha = (m_old == -INFINITY) ? 0.f : expf(m_old - m_new);
                     sc->att_alpha[g] = alpha;
@@ -1386,7 +1457,7 @@ struct Consumer {
                         const int col = nt * 8 + 2 * cq + (i & 1);
                         if (nt < NT && col < 2 * G) oacc[nt][i] *= sc->att_alpha[col % G];
                     }
-                const uint32_t pb = smem_u32(&sc->p_hl[0][0]);
+                const uint32_t pb = smem_u32(&sc->at.p_hl[0][0]);
 #pragma unroll
                 for (int k2 = 0; k2 < kAttnBlock / 16; ++k2) {
                     uint32_t a[4];
@@ -1421,7 +1492,7 @@ struct Consumer {
             if (wc < G) {
                 const int g = wc;
                 float sdot = 0.f;
-                for (int e = lane; e < d; e += 32) sdot = fmaf(sc->q_s[g][e], __uint_as_float((uint32_t)sc->knew[e] << 16), sdot);
+                for (int e = lane; e < d; e += 32) sdot = fmaf(sc->at.q_s[g][e], __uint_as_float((uint32_t)sc->knew[e] << 16), sdot);
                 sdot = warp_sum(sdot);
                 if (lane == 0) {
                     const float m_old = sc->att_m[g], m_new = fmaxf(m_old, sdot);
@@ -1472,30 +1543,40 @@ struct Consumer {
         compute_bar();
         uint32_t *done = p.ctl + p.cl.n_events + b * p.nkv + kvh;
         if (ct == 0) {
-            __threadfence();
-            const uint32_t old = atom_acq_rel_gpu_add(done, 1u);
-            sc->last_flag = (old == (uint32_t)(S - 1)) ? 1u : 0u;
+            const uint32_t old = atom_acq_rel_gpu_add(done, 1u);  // releases the partials written before the barrier
+            sc->last_flag = (old + 1u == (uint32_t)r.n_live) ? 1u : 0u;  // empty splits never arrive
         }
         compute_bar();
         if (sc->last_flag) {
-            // last split of this (sequence, kv head): merge the S partials.
-            // Split weights exp(m_s - M) and 1/L first, then every thread
-            // sums its output pairs over the splits with independent loads.
+            // last split of this (sequence, kv head) to finish: merge the
+            // partials of the live splits.  Split weights exp(m_j - M) and 1/L
+            // first (warp g, lane j: the running max and sum of live split j,
+            // one round trip), then every thread sums its output pairs over
+            // the splits, eight loads in flight at a time.
             if (ct == 0) *done = 0u;  // nothing else touches it in this launch
             const int64_t pbase = ((int64_t)b * p.nkv + kvh) * S * G;
             if (wc < G) {
                 const int g = wc;
                 float M = -INFINITY;
-                for (int s = lane; s < S; s += 32)
-                    M = fmaxf(M, __ldcg(p.attn_part + (pbase + (int64_t)s * G + g) * (d + 2) + d));
-                M = warp_max(M);
+                for (int j0 = 0; j0 < r.n_live; j0 += 32) {
+                    const int j = j0 + lane;
+                    float ms = -INFINITY, ls = 0.f;
+                    if (j < r.n_live) {
+                        const float *src = p.attn_part + (pbase + (int64_t)live_split(r.pos, j, S) * G + g) * (d + 2);
+                        const float2 ml = __ldcg(reinterpret_cast<const float2 *>(src + d));
+                        ms = ml.x;
+                        ls = ml.y;
+                        sc->merge_w[j][g] = ms;  // m_j for now, the weight below
+                        sc->merge_l[j][g] = ls;
+                    }
+                    M = fmaxf(M, warp_max(ms));
+                }
                 float Ls = 0.f;
-                for (int s = lane; s < S; s += 32) {
-                    const float *src = p.attn_part + (pbase + (int64_t)s * G + g) * (d + 2);
-                    const float ms = __ldcg(src + d);
+                for (int j = lane; j < r.n_live; j += 32) {
+                    const float ms = sc->merge_w[j][g];
                     const float w = (ms == -INFINITY) ? 0.f : expf(ms - M);
-                    sc->merge_w[s][g] = w;
-                    Ls = fmaf(__ldcg(src + d + 1), w, Ls);
+                    sc->merge_w[j][g] = w;
+                    Ls = fmaf(sc->merge_l[j][g], w, Ls);
                 }
                 Ls = warp_sum(Ls);
                 if (lane == 0) sc->att_inv_l[g] = 1.f / Ls;
@@ -1510,12 +1591,20 @@ struct Consumer {
                     const float *src = p.attn_part + (pbase + g) * (d + 2) + e;
                     const int64_t sstride = (int64_t)G * (d + 2);
                     float o0 = 0.f, o1 = 0.f;
-#pragma unroll 8
-                    for (int s = 0; s < S; ++s) {
-                        const float2 v = __ldcg(reinterpret_cast<const float2 *>(src + s * sstride));
-                        const float w = sc->merge_w[s][g];
-                        o0 = fmaf(v.x, w, o0);
-                        o1 = fmaf(v.y, w, o1);
+                    constexpr int kChunk = 8;
+                    for (int j0 = 0; j0 < r.n_live; j0 += kChunk) {
+                        float2 v[kChunk];
+#pragma unroll
+                        for (int j = 0; j < kChunk; ++j)
+                            v[j] = (j0 + j < r.n_live)
+                                       ? __ldcg(reinterpret_cast<const float2 *>(src + live_split(r.pos, j0 + j, S) * sstride))
+                                       : make_float2(0.f, 0.f);
+#pragma unroll
+                        for (int j = 0; j < kChunk; ++j) {
+                            const float w = (j0 + j < r.n_live) ? sc->merge_w[j0 + j][g] : 0.f;
+                            o0 = fmaf(v[j].x, w, o0);
+                            o1 = fmaf(v[j].y, w, o1);
+                        }
                     }
                     const float il = sc->att_inv_l[g];
                     const int64_t oi = (int64_t)b * p.nq * d + (int64_t)(kvh * G + g) * d + e;
@@ -1531,10 +1620,8 @@ struct Consumer {
             }
             if (p.tc) fence_proxy_async_global();  // read next by the O projection's TMA
             compute_bar();
-            if (ct == 0 && p.only_op < 0 && t.signal_ev != kNoEvent && !local_abort(c)) {
-                __threadfence();
-                red_release_gpu_add(p.ctl + t.signal_ev, 1u);
-            }
+            if (ct == 0 && p.only_op < 0 && t.signal_ev != kNoEvent && !local_abort(c))
+                red_release_gpu_add(p.ctl + t.signal_ev, 1u);  // cumulative: every row written before the barrier
         }
     }
 };
@@ -1585,10 +1672,10 @@ __device__ void compute_role(const Ctx &c, const Task *q, int nt) {
             cs.full_wait_ns = cs.act_wait_ns = cs.acc_wait_ns = 0;
         }
         if (aborted) return;
-        if (t.op != OP_ATTN && p.only_op < 0 && t.signal_ev != kNoEvent && cs.ct == 0) {
-            __threadfence();
+        // a gpu-scope release is cumulative: it also publishes the other
+        // compute warps' output rows, ordered before it by the barrier above
+        if (t.op != OP_ATTN && p.only_op < 0 && t.signal_ev != kNoEvent && cs.ct == 0)
             red_release_gpu_add(p.ctl + t.signal_ev, 1u);
-        }
     }
 }
 

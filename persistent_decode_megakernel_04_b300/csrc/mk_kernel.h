@@ -54,6 +54,7 @@ struct KParams {
     MvGeom mv[OP_COUNT];
     int32_t slot_bytes, num_slots, attn_ts, attn_splits;  // attn_ts: KV tokens per ring slot
     int32_t l2_prefetch_bytes;
+    int32_t max_inflight;  // ring copies in flight per CTA (0 or >= num_slots: no limit)
     // launch mode
     int32_t only_op;     // -1: every task (persistent mode); else one operator of one layer
     int32_t only_layer;

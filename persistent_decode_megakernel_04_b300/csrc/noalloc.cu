@@ -208,6 +208,7 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_model_cfg *cfg, const mk_we
     k.attn_ts = g.tps;
     k.attn_splits = g.attn_splits;
     k.l2_prefetch_bytes = g.l2_prefetch_bytes;
+    k.max_inflight = g.max_inflight;
     k.only_op = -1;
     k.only_layer = -1;
     k.skip_lm = 0;

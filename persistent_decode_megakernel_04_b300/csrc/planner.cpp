@@ -89,6 +89,9 @@ mk_plan_options resolve_options(const mk_model_cfg &cfg, const mk_plan_options *
     }
     if (o.attn_splits > kMaxSplits) o.attn_splits = kMaxSplits;
     if (o.l2_prefetch_kb < 0) o.l2_prefetch_kb = 0;
+    // batch 1: two copies in flight per CTA stream at full bandwidth and keep
+    // the queue ahead of this SM's other memory requests short
+    if (o.max_inflight <= 0) o.max_inflight = tc ? 0 : 2;
     return o;
 }
 
@@ -130,6 +133,7 @@ mk_status build_plan(const mk_model_cfg &cfg, const mk_plan_options &opt, PlanTa
     if (g.slot_bytes < 2 * d * 2 * 32) return MK_ERR_INVALID;
     g.n_events = 5 * L + (tc ? 1 : 0);
     g.l2_prefetch_bytes = opt.l2_prefetch_kb * 1024;
+    g.max_inflight = opt.max_inflight;
     if (g.tps < 1) return MK_ERR_INVALID;
     if (!tc) {
         g.mv[OP_QKV] = make_geom(H, (nq + 2 * nkv) * d, 1, opt.slot_bytes);

@@ -16,6 +16,7 @@ struct PlanGeom {
     int32_t tps = 0;  // KV tokens per ring slot (divides the 64-token attention block)
     int32_t n_events = 0;
     int32_t l2_prefetch_bytes = 0;
+    int32_t max_inflight = 0;  // ring copies in flight per CTA (0: no limit)
     MvGeom mv[OP_COUNT] = {};
     // batched (tensor-core) path
     bool tc = false;
