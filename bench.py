@@ -254,6 +254,30 @@ def run_mk(args, wl):
     ctx0 = wl.prompt_len + args.warmup + 1  # context length (new token included) of the first timed step
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # The timed steps replay CUDA graphs of the step (the decode launch, then
+    # the greedy pick): a serving loop launches them that way, and for the
+    # small shapes the host's per-launch work would otherwise be what is
+    # timed.  Falls back to direct launches if capture is refused.
+    launch_mode = "eager"
+    g_step = g_pick = None
+    if not args.no_graph:
+        try:
+            g_step, g_pick = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream(dev)
+            cap.wait_stream(stream)
+            with torch.cuda.graph(g_step, stream=cap):
+                plan.decode_step(tok, pos, kv, logits)
+            with torch.cuda.graph(g_pick, stream=cap):
+                plan.greedy_next(logits, tok, pos)
+            stream.wait_stream(cap)
+            torch.cuda.synchronize()
+            plan.check()
+            launch_mode = "cuda graph per step"
+        except Exception as exc:  # capture refused: time direct launches
+            print(f"graph capture unavailable ({exc}); timing direct launches", file=sys.stderr)
+            g_step = g_pick = None
+            torch.cuda.synchronize()
+            plan.check()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -262,9 +286,15 @@ def run_mk(args, wl):
         start.record(stream)
         for i in range(args.steps):
             ev[i][0].record(stream)
-            plan.decode_step(tok, pos, kv, logits)
+            if g_step is not None:
+                g_step.replay()
+            else:
+                plan.decode_step(tok, pos, kv, logits)
             ev[i][1].record(stream)
-            plan.greedy_next(logits, tok, pos)
+            if g_pick is not None:
+                g_pick.replay()
+            else:
+                plan.greedy_next(logits, tok, pos)
         end.record(stream)
         torch.cuda.synchronize()
     if world > 1:
@@ -356,7 +386,7 @@ def run_mk(args, wl):
                        "context": "seeded paged cache" if seeded_context(wl) else "prefilled prompt",
                        "projections": "tcgen05 tiles" if (B > 1 or args.tensor_cores) else "CUDA-core matvec",
                        "ctx_first_timed": ctx0, "ctx_last_timed": ctx0 + args.steps - 1,
-                       "parallelism": f"replicas x{world}",
+                       "parallelism": f"replicas x{world}", "launch": launch_mode,
                        **({"plan_options": kw} if kw else {}),
                        "l2": f"no flush: {weight_bytes_read(m, B) / 1e9:.1f} GB of weights stream per step (> 126 MB L2)"},
             "tokens_per_s": 1e3 / ms_step * B * world,
@@ -395,6 +425,7 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="profiling only: keep the shape, use this many layers")
     ap.add_argument("--tensor-cores", action="store_true",
                     help="run the projections as tcgen05 tiles at batch 1 too (default: CUDA-core matvecs)")
+    ap.add_argument("--no-graph", action="store_true", help="time direct launches instead of CUDA graph replays")
     ap.add_argument("--plan-opt", action="append", default=[], metavar="FIELD=INT",
                     help="set an mk_plan_options field (tuning sweeps), e.g. max_inflight=3")
     ap.add_argument("--trace-out", default="", help="write a per-phase task trace of one extra step here")

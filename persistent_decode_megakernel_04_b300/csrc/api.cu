@@ -43,6 +43,10 @@ struct mk_plan {
     float *d_ssq = nullptr, *d_tc_part = nullptr;
     uint8_t *d_tmaps = nullptr;
     KParams base{};
+    // tensor maps of the last KV cache seen (encoded once per cache, not per step)
+    mk_kv_cache kv_seen{};
+    bool kv_maps_valid = false;
+    alignas(64) uint8_t kv_maps[2][128];
 };
 
 namespace mk {
@@ -118,12 +122,21 @@ mk_status check_weights(const mk_model_cfg &c, const mk_weight_ptrs *w) {
     return MK_OK;
 }
 
-mk_status check_kv(const mk_plan *p, const mk_kv_cache *kv) {
+// Validates the cache and keeps its two tensor maps in the plan: they are
+// encoded again only when the pools or their page counts change.
+mk_status check_kv(mk_plan *p, const mk_kv_cache *kv) {
     if (!kv || !aligned16(kv->k_pool) || !aligned16(kv->v_pool) || !aligned16(kv->page_table)) return MK_ERR_INVALID;
     if (kv->num_pages <= 0 || kv->max_pages_per_seq <= 0) return MK_ERR_INVALID;
     if ((int64_t)kv->max_pages_per_seq * p->cfg.page_size < p->cfg.max_seq) return MK_ERR_INVALID;
+    const mk_kv_cache &s = p->kv_seen;
+    if (p->kv_maps_valid && s.k_pool == kv->k_pool && s.v_pool == kv->v_pool && s.num_pages == kv->num_pages)
+        return MK_OK;
     KParams probe{};
+    p->kv_maps_valid = false;
     if (!encode_kv_maps(probe, p->cfg, *kv, p->tables.g.tps)) return MK_ERR_INVALID;  // pools too large for a map
+    std::memcpy(p->kv_maps, probe.kv_maps, sizeof(p->kv_maps));
+    p->kv_seen = *kv;
+    p->kv_maps_valid = true;
     return MK_OK;
 }
 
@@ -143,7 +156,7 @@ void free_plan(mk_plan *p) {
 KParams step_params(const mk_plan *p, const int32_t *tokens, int32_t tok_stride, const int32_t *positions,
                     int32_t pos_stride, const mk_kv_cache *kv, float *logits) {
     KParams k = p->base;
-    encode_kv_maps(k, p->cfg, *kv, p->tables.g.tps);  // checked by check_kv
+    std::memcpy(k.kv_maps, p->kv_maps, sizeof(k.kv_maps));  // encoded by check_kv
     k.k_pool = static_cast<uint16_t *>(kv->k_pool);
     k.v_pool = static_cast<uint16_t *>(kv->v_pool);
     k.page_table = kv->page_table;
