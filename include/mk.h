@@ -105,7 +105,9 @@ typedef struct {
     int32_t num_slots;     /* ring slots (default 6) */
     int32_t timeout_ms;    /* budget of every device wait (default 2000) */
     uint32_t planner_seed; /* nonzero: permute the CTA <-> tile assignment */
-    int32_t l2_prefetch_kb;/* per-CTA L2 prefetch distance ahead of the ring (default 0 = off) */
+    int32_t l2_prefetch_kb;/* batch 1: on reaching an O projection, prefetch into L2 up to this many
+                              KB of the weights the ring cannot hold yet (the O rows past the ring,
+                              then the first gate/up rows); default 0 = off (measured slower) */
     int32_t test_unreachable_event; /* failure-path testing: k > 0 makes the waiters of event k-1
                                        need one signal more than can ever arrive, so their
                                        bounded wait expires and the step reports MK_ERR_TIMEOUT */

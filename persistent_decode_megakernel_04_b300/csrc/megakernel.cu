@@ -404,6 +404,36 @@ struct Producer {
         return true;
     }
 
+    // Batch 1, on reaching an O projection task: while the attention phase
+    // holds the compute warps, the ring fills with O rows and the weight
+    // stream would stop.  Prefetch into L2 (up to l2_prefetch_bytes) the O
+    // rows the ring cannot hold, then the first gate/up rows of the next
+    // task, so that HBM keeps working and those copies later hit L2.
+    __device__ void prefetch_past_attention(const Ctx &c, const Task &t, const Task *next) {
+        const KParams &p = *c.p;
+        int64_t budget = p.l2_prefetch_bytes;
+        const int64_t ring = (int64_t)ns * slot_bytes;
+        const int64_t rowb_o = (int64_t)p.mv[OP_O].K * 2;
+        const char *ob = reinterpret_cast<const char *>(p.layers[t.layer].wo) + (int64_t)t.a0 * rowb_o;
+        const int64_t obytes = (int64_t)(t.a1 - t.a0) * rowb_o;
+        for (int64_t off = ring; off < obytes && budget > 0; off += 32768) {
+            const int64_t n = min(min((int64_t)32768, obytes - off), budget);
+            prefetch_l2(ob + off, (uint32_t)n);
+            budget -= n;
+        }
+        if (next == nullptr || next->op != OP_GU || !task_active(p, *next) || budget <= 0) return;
+        const int64_t rowb = (int64_t)p.mv[OP_GU].K * 2;
+        const int64_t rows = min((int64_t)(next->a1 - next->a0), budget / (2 * rowb));
+        const LayerW &lw = p.layers[next->layer];
+        const char *gb = reinterpret_cast<const char *>(lw.w_gate) + (int64_t)next->a0 * rowb;
+        const char *ub = reinterpret_cast<const char *>(lw.w_up) + (int64_t)next->a0 * rowb;
+        for (int64_t off = 0; off < rows * rowb; off += 32768) {
+            const uint32_t n = (uint32_t)min((int64_t)32768, rows * rowb - off);
+            prefetch_l2(gb + off, n);
+            prefetch_l2(ub + off, n);
+        }
+    }
+
     // KV of one 64-token block: TMA tiles of ts tokens x 64 columns (128-byte
     // swizzle) from the paged pools, K halves then V halves, in 64/ts slots.
     __device__ bool run_attn(const Ctx &c, const Task &t) {
@@ -485,6 +515,8 @@ __device__ void producer_role(const Ctx &c, const Task *q, int nt) {
         if (!task_active(*c.p, t)) continue;
         pr.tr = trace_slot(*c.p, i);
         bool ok = true;
+        if (t.op == OP_O && !c.p->tc && c.p->l2_prefetch_bytes > 0)
+            pr.prefetch_past_attention(c, t, i + 1 < nt ? &q[i + 1] : nullptr);
         if (t.op == OP_ATTN) ok = pr.run_attn(c, t);
         else if (t.op == OP_EMBED) ok = true;
         else ok = c.p->tc ? pr.run_gemm(c, t) : pr.run_matvec(c, t);
