@@ -313,20 +313,11 @@ struct Producer {
     uint32_t ns = 0;         // ring slots (kept in a register)
     uint32_t slot_bytes = 0;
     uint32_t fmax = 0;       // copies in flight at most (0: every free slot)
-    // deferred L2 prefetch (see prefetch_past_attention): armed on reaching an
-    // O task, fired once the ring is full and the task before O was released
-    const Task *pf_task = nullptr, *pf_next = nullptr;
-    uint32_t pf_after = 0;
 
     __device__ bool acquire_slot(const Ctx &c, uint32_t *slot) {
         const uint32_t s = issued % ns;
         const uint32_t round = issued / ns;
         const uint64_t t0 = tr ? globaltimer_ns() : 0;
-        if (pf_task != nullptr && !mbar_try_wait(&c.sc->empty[s], (round & 1u) ^ 1u) &&
-            ld_acquire_cta(&c.sc->ready) >= pf_after) {
-            prefetch_past_attention(c, *pf_task, pf_next);
-            pf_task = nullptr;
-        }
         if (!wait_mbar(c, &c.sc->empty[s], (round & 1u) ^ 1u, SITE_EMPTY_WAIT)) return false;
         if (fmax != 0 && issued >= fmax) {
             // copy number issued - fmax must have landed: fewer bytes queued
@@ -413,10 +404,10 @@ struct Producer {
         return true;
     }
 
-    // Batch 1, while loading an O projection task: once the ring is full and
-    // the attention phase has begun, the weight stream would stop until the
-    // compute warps reach O.  Prefetch into L2 (up to l2_prefetch_bytes) the
-    // O rows the ring cannot hold, then the first gate/up rows of the next
+    // Batch 1, on reaching an O projection task: while the attention phase
+    // holds the compute warps, the ring fills with O rows and the weight
+    // stream would stop.  Prefetch into L2 (up to l2_prefetch_bytes) the O
+    // rows the ring cannot hold, then the first gate/up rows of the next
     // task, so that HBM keeps working and those copies later hit L2.
     __device__ void prefetch_past_attention(const Ctx &c, const Task &t, const Task *next) {
         const KParams &p = *c.p;
@@ -524,15 +515,11 @@ __device__ void producer_role(const Ctx &c, const Task *q, int nt) {
         if (!task_active(*c.p, t)) continue;
         pr.tr = trace_slot(*c.p, i);
         bool ok = true;
-        if (t.op == OP_O && !c.p->tc && c.p->l2_prefetch_bytes > 0) {
-            pr.pf_task = &q[i];
-            pr.pf_next = i + 1 < nt ? &q[i + 1] : nullptr;
-            pr.pf_after = (uint32_t)i;  // the task before O (attention) has been released
-        }
+        if (t.op == OP_O && !c.p->tc && c.p->l2_prefetch_bytes > 0)
+            pr.prefetch_past_attention(c, t, i + 1 < nt ? &q[i + 1] : nullptr);
         if (t.op == OP_ATTN) ok = pr.run_attn(c, t);
         else if (t.op == OP_EMBED) ok = true;
         else ok = c.p->tc ? pr.run_gemm(c, t) : pr.run_matvec(c, t);
-        pr.pf_task = nullptr;  // a prefetch not fired during its O task is dropped
         if (!ok) break;
     }
     pr.drain(c);
