@@ -38,6 +38,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "mk_kernel.h"
 #include "ptx.cuh"
 
@@ -49,7 +51,7 @@ namespace {
 // for its per-warp row totals (a CTA runs one task at a time).
 struct AttnScratch {
     alignas(16) float q_s[kMaxGroup][kMaxHeadDim];        // RoPE'd, scaled queries (fp32)
-    alignas(16) float s_s[kMaxGroup][kAttnBlock];         // scores of one 64-token block
+    alignas(16) float s_s[kMaxGroup][kAttnStep];          // scores of one step (up to two 64-token blocks)
     alignas(16) uint16_t q_hl[2 * kMaxGroup][kQhlStride];  // queries as bf16 high parts, then low parts
     alignas(16) uint16_t p_hl[2 * kMaxGroup][kPhlStride];  // softmax weights, bf16 high then low parts
 };
@@ -1319,6 +1321,15 @@ struct Consumer {
                (uint32_t)((((kv * halves + h) * 128) << ts_log2) + ti * 128 + ((ch ^ (ti & 7)) << 4) + (e & 7) * 2);
     }
 
+    // The same for the tokens of an attention step held in up to four slots
+    // (token tok of the step lies in slot tok >> ts_log2).
+    __device__ static __forceinline__ uint32_t kv_elem4(uint32_t sb0, uint32_t sb1, uint32_t sb2, uint32_t sb3,
+                                                        int ts_log2, int halves, int kv, int tok, int e) {
+        const int sl = tok >> ts_log2;
+        const uint32_t lo = (sl & 1) ? sb1 : sb0, hi = (sl & 1) ? sb3 : sb2;
+        return kv_elem((sl & 2) ? hi : lo, 0u, ts_log2, halves, kv, tok & ((1 << ts_log2) - 1), e);
+    }
+
     __device__ void run_attn(const Ctx &c, const Task &t) {
         const KParams &p = *c.p;
         SmemCtl *sc = c.sc;
@@ -1417,21 +1428,31 @@ struct Consumer {
         const bool head_lane = (G == 8) || (G == 1 ? cq == 0 : cq < G / 2);
         float oacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 
-        for (int32_t blk = r.blo; blk < r.bhi; ++blk) {
+        // One step: NB (1 or 2) consecutive 64-token blocks, held in NB * nsl
+        // ring slots.  Two blocks per step halve the barriers per token and
+        // put all 8 warps on the scores (16 tokens each).
+        auto attend = [&](auto nb_const, int32_t blk) {
+            constexpr int NB = decltype(nb_const)::value;
+            const int nslots = NB * nsl;
             const uint64_t tb0 = tracing ? globaltimer_ns() : 0;
             const uint32_t sid0 = wait_slot_at(c, consumed);
-            const uint32_t sid1 = (nsl == 2) ? wait_slot_at(c, consumed + 1u) : sid0;
+            const uint32_t sid1 = (nslots > 1) ? wait_slot_at(c, consumed + 1u) : sid0;
+            const uint32_t sid2 = (nslots > 2) ? wait_slot_at(c, consumed + 2u) : sid0;
+            const uint32_t sid3 = (nslots > 3) ? wait_slot_at(c, consumed + 3u) : sid0;
             const uint32_t sb0 = smem_u32(c.ring + (size_t)sid0 * slot_bytes);
             const uint32_t sb1 = smem_u32(c.ring + (size_t)sid1 * slot_bytes);
+            const uint32_t sb2 = smem_u32(c.ring + (size_t)sid2 * slot_bytes);
+            const uint32_t sb3 = smem_u32(c.ring + (size_t)sid3 * slot_bytes);
             const int32_t tok0 = blk * kAttnBlock;
-            // scores of tokens 16 wc .. 16 wc + 15
-            if (wc < 4) {
+            // scores of tokens 16 wc .. 16 wc + 15 of the step
+            if (wc < 4 * NB) {
                 float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     if (ks < nks) {
                         uint32_t a[4], qf[2];
-                        ldsm_x4(a, kv_elem(sb0, sb1, ts_log2, halves, 0, 16 * wc + (lane & 15), ks * 16 + (lane >> 4) * 8));
+                        ldsm_x4(a, kv_elem4(sb0, sb1, sb2, sb3, ts_log2, halves, 0, 16 * wc + (lane & 15),
+                                            ks * 16 + (lane >> 4) * 8));
 #pragma unroll
                         for (int nt = 0; nt < 2; ++nt) {
                             if (nt < NT) {
@@ -1460,17 +1481,25 @@ struct Consumer {
             // online softmax, warp g for head g: weights as bf16 high / low parts
             if (wc < G) {
                 const int g = wc;
-                const float s0 = sc->at.s_s[g][lane], s1 = sc->at.s_s[g][lane + 32];
+                float sv[2 * NB], pv[2 * NB];
+                float mx = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < 2 * NB; ++j) {
+                    sv[j] = sc->at.s_s[g][lane + 32 * j];
+                    mx = fmaxf(mx, sv[j]);
+                }
                 const float m_old = sc->att_m[g];
-                const float m_new = fmaxf(m_old, warp_max(fmaxf(s0, s1)));
-                const float p0 = (s0 == -INFINITY) ? 0.f : expf(s0 - m_new);
-                const float p1 = (s1 == -INFINITY) ? 0.f : expf(s1 - m_new);
-                const float sum = warp_sum(p0 + p1);
-                const uint16_t h0 = f32_to_bf16_bits(p0), h1 = f32_to_bf16_bits(p1);
-                sc->at.p_hl[g][lane] = h0;
-                sc->at.p_hl[g][lane + 32] = h1;
-                sc->at.p_hl[G + g][lane] = f32_to_bf16_bits(p0 - __uint_as_float((uint32_t)h0 << 16));
-                sc->at.p_hl[G + g][lane + 32] = f32_to_bf16_bits(p1 - __uint_as_float((uint32_t)h1 << 16));
+                const float m_new = fmaxf(m_old, warp_max(mx));
+                float psum = 0.f;
+#pragma unroll
+                for (int j = 0; j < 2 * NB; ++j) {
+                    pv[j] = (sv[j] == -INFINITY) ? 0.f : expf(sv[j] - m_new);
+                    psum += pv[j];
+                    const uint16_t h = f32_to_bf16_bits(pv[j]);
+                    sc->at.p_hl[g][lane + 32 * j] = h;
+                    sc->at.p_hl[G + g][lane + 32 * j] = f32_to_bf16_bits(pv[j] - __uint_as_float((uint32_t)h << 16));
+                }
+                const float sum = warp_sum(psum);
                 if (lane == 0) {
                     const float alpha = (m_old == -INFINITY) ? 0.f : expf(m_old - m_new);
                     sc->att_alpha[g] = alpha;
@@ -1491,11 +1520,11 @@ struct Consumer {
                     }
                 const uint32_t pb = smem_u32(&sc->at.p_hl[0][0]);
 #pragma unroll
-                for (int k2 = 0; k2 < kAttnBlock / 16; ++k2) {
+                for (int k2 = 0; k2 < NB * kAttnBlock / 16; ++k2) {
                     uint32_t a[4];
                     const int q = lane >> 3;
-                    ldsm_x4_trans(a, kv_elem(sb0, sb1, ts_log2, halves, 1, k2 * 16 + (q >> 1) * 8 + (lane & 7),
-                                             16 * wc + (q & 1) * 8));
+                    ldsm_x4_trans(a, kv_elem4(sb0, sb1, sb2, sb3, ts_log2, halves, 1,
+                                              k2 * 16 + (q >> 1) * 8 + (lane & 7), 16 * wc + (q & 1) * 8));
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt) {
                         if (nt < NT) {
@@ -1507,18 +1536,25 @@ struct Consumer {
                     }
                 }
             }
-            compute_bar();  // the block's slots, scores and weights are free
+            compute_bar();  // the step's slots, scores and weights are free
             if (ct == 0) {
                 const uint32_t na = p.tc ? 1u : (uint32_t)kComputeWarps;
                 mbar_arrive_n(&sc->empty[sid0], na);
-                if (nsl == 2) mbar_arrive_n(&sc->empty[sid1], na);
+                if (nslots > 1) mbar_arrive_n(&sc->empty[sid1], na);
+                if (nslots > 2) mbar_arrive_n(&sc->empty[sid2], na);
+                if (nslots > 3) mbar_arrive_n(&sc->empty[sid3], na);
             }
-            consumed += (uint32_t)nsl;
+            consumed += (uint32_t)nslots;
             if (tracing) {
                 act_wait_ns += tb1 - tb0;            // slot waits + scores
                 acc_wait_ns += globaltimer_ns() - tb2;  // value sums
             }
-        }
+        };
+        // pairs of blocks while the ring can hold both at once, then the rest
+        int32_t blk = r.blo;
+        if (ns >= (uint32_t)(2 * nsl))
+            for (; blk + 1 < r.bhi; blk += 2) attend(std::integral_constant<int, 2>{}, blk);
+        for (; blk < r.bhi; ++blk) attend(std::integral_constant<int, 1>{}, blk);
         if (r.has_new) {
             // the new token, from shared memory: one more online-softmax step
             if (wc < G) {

@@ -19,7 +19,8 @@ constexpr int kMaxGroup = 8;      // q heads per kv head
 constexpr int kMaxHeadDim = 128;
 constexpr int kAttnBlock = 64;    // cached tokens per attention block (one aligned run of a page)
 constexpr int kQhlStride = kMaxHeadDim + 8;  // bf16 row stride of the split queries (conflict-free ldmatrix)
-constexpr int kPhlStride = kAttnBlock + 8;   // bf16 row stride of the split softmax weights
+constexpr int kAttnStep = 2 * kAttnBlock;    // cached tokens an attention step handles at most
+constexpr int kPhlStride = kAttnStep + 8;    // bf16 row stride of the split softmax weights
 constexpr int kMaxResid = 512;    // residual rows prefetched per matvec task
 constexpr int kMvResident = 2;    // matvec inputs of up to 2 x 2048 columns stay in registers
 constexpr int kMvAhead = 3;       // longer inputs: pieces loaded this many slots ahead
