@@ -224,3 +224,17 @@ def test_tiny_variants_group_sizes_and_head_dim(cuda_device, m):
     plan, kv = harness.gpu_plan(m, 128)
     model = harness.oracle_model(m)
     harness.run_teacher_forced(plan, kv, model, synth.tokens(70, 0, 8, m.vocab), 4, 128)
+
+
+@pytest.mark.parametrize("opts", [dict(max_inflight=1, attn_splits=1),
+                                  dict(max_inflight=6, attn_splits=2, l2_prefetch_kb=256),
+                                  dict(num_slots=3, slot_bytes=8192, attn_splits=1)],
+                         ids=["inflight1", "uncapped-prefetch", "no-two-block-steps"])
+def test_tiny_ring_and_attention_step_options(cuda_device, opts):
+    """Ring copies capped at one in flight or uncapped, the optional L2
+    prefetch, and attention taking both two-block and one-block steps (three
+    cached blocks in one split; one and two blocks in two splits), or only
+    one-block steps when the ring cannot hold two blocks at once."""
+    plan, kv = harness.gpu_plan(TINY, 256, opts=mk.mk_plan_options(**opts))
+    model = harness.oracle_model(TINY)
+    harness.run_teacher_forced(plan, kv, model, synth.tokens(150, 0, 9, TINY.vocab), 4, 256)
