@@ -258,10 +258,24 @@ def run_mk(args, wl):
     ctx0 = wl.prompt_len + args.warmup + 1  # context length (new token included) of the first timed step
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    # The timed steps replay CUDA graphs of the step (the decode launch, then
-    # the greedy pick): a serving loop launches them that way, and for the
-    # small shapes the host's per-launch work would otherwise be what is
-    # timed.  Falls back to direct launches if capture is refused.
+    # The timed steps replay CUDA graphs of the step: a serving loop launches
+    # it that way, and for the small shapes the host's per-launch work would
+    # otherwise be what is timed.  At batch 1 the greedy pick runs inside the
+    # decode launch (mk_decode_step_greedy); batched plans, or
+    # --separate-pick, time the decode launch and then mk_greedy_next.
+    # Falls back to direct launches if capture is refused.
+    fused = B == 1 and not args.tensor_cores and not args.separate_pick
+
+    def step_decode():
+        if fused:
+            plan.decode_step_greedy(tok, pos, kv, logits)
+        else:
+            plan.decode_step(tok, pos, kv, logits)
+
+    def step_pick():
+        if not fused:
+            plan.greedy_next(logits, tok, pos)
+
     launch_mode = "eager"
     g_step = g_pick = None
     if not args.no_graph:
@@ -270,9 +284,12 @@ def run_mk(args, wl):
             cap = torch.cuda.Stream(dev)
             cap.wait_stream(stream)
             with torch.cuda.graph(g_step, stream=cap):
-                plan.decode_step(tok, pos, kv, logits)
-            with torch.cuda.graph(g_pick, stream=cap):
-                plan.greedy_next(logits, tok, pos)
+                step_decode()
+            if fused:
+                g_pick = None
+            else:
+                with torch.cuda.graph(g_pick, stream=cap):
+                    step_pick()
             stream.wait_stream(cap)
             torch.cuda.synchronize()
             plan.check()
@@ -293,12 +310,12 @@ def run_mk(args, wl):
             if g_step is not None:
                 g_step.replay()
             else:
-                plan.decode_step(tok, pos, kv, logits)
+                step_decode()
             ev[i][1].record(stream)
             if g_pick is not None:
                 g_pick.replay()
             else:
-                plan.greedy_next(logits, tok, pos)
+                step_pick()
         end.record(stream)
         torch.cuda.synchronize()
     if world > 1:
@@ -391,6 +408,7 @@ def run_mk(args, wl):
                        "projections": "tcgen05 tiles" if (B > 1 or args.tensor_cores) else "CUDA-core matvec",
                        "ctx_first_timed": ctx0, "ctx_last_timed": ctx0 + args.steps - 1,
                        "parallelism": f"replicas x{world}", "launch": launch_mode,
+                       "greedy_pick": "in the decode launch" if fused else "separate kernel",
                        **({"plan_options": kw} if kw else {}),
                        "l2": f"no flush: {weight_bytes_read(m, B) / 1e9:.1f} GB of weights stream per step (> 126 MB L2)"},
             "tokens_per_s": 1e3 / ms_step * B * world,
@@ -403,7 +421,7 @@ def run_mk(args, wl):
             "clocks": clk,
             "e2e": {"value": e2e_ms / B, "unit": "ms/token", "h2d_bytes_per_step": 8 * B,
                     "d2h_bytes_per_step": 4 * B * m.vocab},
-            "gpu_launches": 2 * args.steps,
+            "gpu_launches": (1 if fused else 2) * args.steps,
             "ablation": abl,
             "cpu_baseline": cpu,
         }
@@ -430,6 +448,8 @@ def main():
     ap.add_argument("--tensor-cores", action="store_true",
                     help="run the projections as tcgen05 tiles at batch 1 too (default: CUDA-core matvecs)")
     ap.add_argument("--no-graph", action="store_true", help="time direct launches instead of CUDA graph replays")
+    ap.add_argument("--separate-pick", action="store_true",
+                    help="batch 1: time the decode launch and mk_greedy_next instead of the fused pick")
     ap.add_argument("--plan-opt", action="append", default=[], metavar="FIELD=INT",
                     help="set an mk_plan_options field (tuning sweeps), e.g. max_inflight=3")
     ap.add_argument("--trace-out", default="", help="write a per-phase task trace of one extra step here")

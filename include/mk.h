@@ -168,6 +168,18 @@ mk_status mk_prefill(mk_plan *plan, const int32_t *tokens, int32_t T, const mk_k
  * (lowest index on ties) and positions[b] += 1, on the device. */
 mk_status mk_greedy_next(mk_plan *plan, const float *logits, int32_t *tokens, int32_t *positions, void *stream);
 
+/* One decode step followed by the greedy pick, in place: tokens[b] becomes
+ * the argmax of row b of logits (the lowest index among equal maxima; NaN
+ * never wins, and a row without a finite maximum gives 0x7FFFFFFF) and
+ * positions[b] is incremented, exactly as mk_decode_step then
+ * mk_greedy_next.  At batch 1 the pick runs inside the decode launch (each
+ * CTA's maximum over its LM-head rows, merged with one 64-bit atomic max);
+ * batched plans launch the pick after the step.  tokens and positions are
+ * device arrays [batch], read by the step and rewritten after it; logits are
+ * still written.  Errors as mk_decode_step. */
+mk_status mk_decode_step_greedy(mk_plan *plan, int32_t *tokens, int32_t *positions, const mk_kv_cache *kv,
+                                float *logits, void *stream);
+
 /* Task trace of the last step run with a plan created with options.trace:
  * for every CTA c and queue position i (the order of mk_plan_describe),
  * out[(c * *max_tasks + i) * 8 + k] holds, in globaltimer nanoseconds,

@@ -58,7 +58,8 @@ class mk_task_info(ctypes.Structure):
 _lib = None
 EXPORTS = ("mk_plan_create", "mk_plan_create_ex", "mk_decode_step", "mk_decode_step_ablation",
            "mk_decode_step_host", "mk_prefill", "mk_greedy_next", "mk_plan_last_error", "mk_status_string",
-           "mk_error_site_string", "mk_plan_destroy", "mk_plan_describe", "mk_plan_trace", "mk_decode_step_noalloc")
+           "mk_error_site_string", "mk_plan_destroy", "mk_plan_describe", "mk_plan_trace", "mk_decode_step_noalloc",
+           "mk_decode_step_greedy")
 
 
 def lib():
@@ -73,6 +74,7 @@ def lib():
         step = [_vp, _vp, _vp, P(mk_kv_cache), _vp, _vp]
         L.mk_decode_step.argtypes = step
         L.mk_decode_step_ablation.argtypes = step
+        L.mk_decode_step_greedy.argtypes = step
         L.mk_decode_step_host.argtypes = step
         L.mk_prefill.argtypes = [_vp, _vp, _i32, P(mk_kv_cache), _vp, _vp]
         L.mk_greedy_next.argtypes = [_vp, _vp, _vp, _vp, _vp]
@@ -201,6 +203,11 @@ class Plan:
     def decode_step(self, tokens, positions, kv: KVCache, logits, stream=None):
         _check(lib().mk_decode_step(self.h, tokens.data_ptr(), positions.data_ptr(), ctypes.byref(kv.desc),
                                     logits.data_ptr(), _stream_ptr(stream)), "mk_decode_step")
+
+    def decode_step_greedy(self, tokens, positions, kv: KVCache, logits, stream=None):
+        """A decode step, then tokens = argmax(logits), positions += 1 in place."""
+        _check(lib().mk_decode_step_greedy(self.h, tokens.data_ptr(), positions.data_ptr(), ctypes.byref(kv.desc),
+                                           logits.data_ptr(), _stream_ptr(stream)), "mk_decode_step_greedy")
 
     def decode_step_ablation(self, tokens, positions, kv: KVCache, logits, stream=None):
         _check(lib().mk_decode_step_ablation(self.h, tokens.data_ptr(), positions.data_ptr(), ctypes.byref(kv.desc),

@@ -306,7 +306,7 @@ mk_status mk_plan_create_ex(const mk_model_cfg *cfg, const mk_weight_ptrs *w, co
     const mk_model_cfg &c = *cfg;
     const int32_t G = c.n_q_heads / c.n_kv_heads, S = g.attn_splits;
     const int32_t qkv_rows = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
-    p->cl = ctl_layout(g.n_events, c.batch * c.n_kv_heads, g.tc ? g.n_tile_ctrs : 0);
+    p->cl = ctl_layout(g.n_events, c.batch * c.n_kv_heads, g.tc ? g.n_tile_ctrs : 0, c.batch);
     const size_t n_part = (size_t)c.batch * c.n_kv_heads * S * G * (c.head_dim + 2);
     if ((st = dev_alloc(p, &p->d_layers, c.n_layers)) || (st = dev_alloc(p, &p->d_tasks, p->tables.tasks.size())) ||
         (st = dev_alloc(p, &p->d_queue, p->tables.queue_off.size())) ||
@@ -477,6 +477,23 @@ mk_status mk_decode_step(mk_plan *p, const int32_t *tokens, const int32_t *posit
     if (st != MK_OK) return st;
     KParams k = step_params(p, tokens, 1, positions, 1, kv, logits);
     return launch_step(p, k, static_cast<cudaStream_t>(stream));
+}
+
+mk_status mk_decode_step_greedy(mk_plan *p, int32_t *tokens, int32_t *positions, const mk_kv_cache *kv,
+                                float *logits, void *stream) {
+    if (!p || !tokens || !positions || !logits) return MK_ERR_INVALID;
+    mk_status st = check_kv(p, kv);
+    if (st != MK_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    KParams k = step_params(p, tokens, 1, positions, 1, kv, logits);
+    if (!p->tables.g.tc) {
+        k.greedy = 1;
+        k.next_tokens = tokens;
+        k.next_positions = positions;
+        return launch_step(p, k, s);
+    }
+    if ((st = launch_step(p, k, s)) != MK_OK) return st;
+    return cuda_status(launch_greedy_next(logits, p->cfg.batch, p->cfg.vocab, tokens, positions, s));
 }
 
 mk_status mk_decode_step_ablation(mk_plan *p, const int32_t *tokens, const int32_t *positions,

@@ -68,6 +68,7 @@ struct SmemCtl {
     uint32_t last_flag;  // attention: this CTA finished the last split of a head
     uint32_t pad0;
     float rms_part[kComputeWarps];
+    unsigned long long amax_part[kComputeWarps];  // fused greedy pick: each warp's packed maximum
     float att_m[kMaxGroup], att_l[kMaxGroup], att_alpha[kMaxGroup];
     float att_inv_l[kMaxGroup];
     float merge_w[kMaxSplits][kMaxGroup];  // live split j's weight exp(m_j - max m) in the merge
@@ -110,6 +111,17 @@ struct Ctx {
     uint8_t *aring;  // activation ring (batched path)
     int cta;
 };
+
+// A logit and its row as one 64-bit word whose unsigned order is the pick's:
+// the larger logit, then the lower row.  Only finite values and +inf take
+// part (as in a strictly-greater scan from -inf, NaN never wins); 0 means
+// no candidate.
+__device__ __forceinline__ unsigned long long pack_logit(float x, int32_t row) {
+    if (!(x > -INFINITY)) return 0ull;
+    const uint32_t u = __float_as_uint(x);
+    const uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)row);
+}
 
 __device__ __forceinline__ bool is_proj(int op) { return op == OP_QKV || op == OP_O || op == OP_GU || op == OP_DOWN || op == OP_LM; }
 
@@ -931,6 +943,7 @@ struct Consumer {
         float *const out_qkv = p.qkv, *const out_x = p.x, *const out_h = p.hbuf, *const out_logits = p.logits;
         const uint16_t *const embed_row = p.embed + (int64_t)token * p.H;
         int32_t pg = 0;  // row groups waiting in mv_part
+        unsigned long long best = 0ull;  // fused greedy pick: this thread's best packed logit
         for (int32_t row = t.a0; row < t.a1;) {
             int32_t n = min(g.rpp, t.a1 - row);
             if (op == OP_QKV) n = min(n, (row < qb1 ? qb1 : (row < qb2 ? qb2 : qb3)) - row);
@@ -989,9 +1002,25 @@ struct Consumer {
             row += n;
             if (pg == kPartGroups || row >= t.a1) {
                 compute_bar();  // every warp's totals of the waiting groups are in
-                mv_finish(c, t, g, pg, resid_in_smem, out_qkv, out_x, out_h, out_logits, embed_row);
+                mv_finish(c, t, g, pg, resid_in_smem, out_qkv, out_x, out_h, out_logits, embed_row, best);
                 pg = 0;
                 if (row < t.a1) compute_bar();  // the buffer is refilled
+            }
+        }
+        if (op == OP_LM && p.greedy) {
+            // fused greedy pick: this CTA's best (logit, row), then one 64-bit
+            // max per CTA; the last CTA out writes the token
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+                best = other > best ? other : best;
+            }
+            if (lane == 0) c.sc->amax_part[wc] = best;
+            compute_bar();
+            if (ct == 0) {
+                for (int w = 1; w < kComputeWarps; ++w) best = c.sc->amax_part[w] > best ? c.sc->amax_part[w] : best;
+                if (best != 0ull)
+                    atomicMax(reinterpret_cast<unsigned long long *>(p.ctl + p.cl.amax_idx), best);
             }
         }
     }
@@ -1001,7 +1030,8 @@ struct Consumer {
     // SiLU(gate) * up, or the raw value).
     __device__ __forceinline__ void mv_finish(const Ctx &c, const Task &t, const MvGeom &g, int32_t pg,
                                               bool resid_in_smem, float *out_qkv, float *out_x, float *out_h,
-                                              float *out_logits, const uint16_t *embed_row) const {
+                                              float *out_logits, const uint16_t *embed_row,
+                                              unsigned long long &best) const {
         const int op = t.op;
         for (int32_t i = ct; i < pg * 8; i += kComputeThreads) {
             const int32_t gi = i >> 3, ri = i & 7;
@@ -1030,7 +1060,12 @@ struct Consumer {
                     out_x[orow] = xo + tot;
                     break;
                 }
-                default: out_logits[orow] = tot; break;
+                default: {
+                    out_logits[orow] = tot;
+                    const unsigned long long w = pack_logit(tot, orow);
+                    best = w > best ? w : best;
+                    break;
+                }
             }
         }
     }
@@ -1840,6 +1875,14 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant_
         if (old == gridDim.x - 1) {
             for (int i = 0; i < p.cl.n_events + p.cl.n_done; ++i) p.ctl[i] = 0u;
             *ex = 0u;
+            if (p.greedy && !p.skip_lm && (p.only_op < 0 || p.only_op == OP_LM) && !global_abort(p)) {
+                // fused greedy pick (batch 1): every CTA's maximum is in
+                unsigned long long *am = reinterpret_cast<unsigned long long *>(p.ctl + p.cl.amax_idx);
+                const unsigned long long w = __ldcg(am);
+                p.next_tokens[0] = (w == 0ull) ? 0x7FFFFFFF : (int32_t)(0xFFFFFFFFu - (uint32_t)w);
+                p.next_positions[0] += 1;
+                *am = 0ull;
+            }
             __threadfence();
         }
     }

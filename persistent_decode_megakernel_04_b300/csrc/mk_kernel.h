@@ -60,6 +60,10 @@ struct KParams {
     int32_t only_op;     // -1: every task (persistent mode); else one operator of one layer
     int32_t only_layer;
     int32_t skip_lm;     // prefill positions before the last: no LM head
+    // batch 1, fused greedy pick: after the LM head, next_tokens[0] = argmax
+    // of the logits (lowest index among equal maxima), next_positions[0] += 1
+    int32_t greedy;
+    int32_t *next_tokens, *next_positions;
     uint64_t timeout_ns;
     // optional task trace: [num_ctas][trace_stride][8] globaltimer stamps
     uint64_t *trace;

@@ -94,16 +94,18 @@ enum ErrSite : int32_t {
 //   [0, n_events)                           event counters
 //   [n_events, n_events + batch*n_kv_heads) attention split-done counters
 //   then n_tiles row-tile counters (batched path), then: exit counter, abort
-//   flag, error status, error site, error cta, error detail
+//   flag, error status, error site, error cta, error detail, then one 64-bit
+//   word per sequence (even index): the fused greedy pick's packed maximum
 struct CtlLayout {
     int32_t n_events;
     int32_t n_done;
     int32_t tile_idx, n_tiles;
     int32_t exit_idx, abort_idx, err_idx;
+    int32_t amax_idx;  // sequence b's packed (logit, index) maximum: words amax_idx + 2b, + 2b + 1
     int32_t total;
 };
 
-inline CtlLayout ctl_layout(int32_t n_events, int32_t n_done, int32_t n_tiles) {
+inline CtlLayout ctl_layout(int32_t n_events, int32_t n_done, int32_t n_tiles, int32_t n_seq) {
     CtlLayout c;
     c.n_events = n_events;
     c.n_done = n_done;
@@ -112,7 +114,8 @@ inline CtlLayout ctl_layout(int32_t n_events, int32_t n_done, int32_t n_tiles) {
     c.exit_idx = c.tile_idx + n_tiles;
     c.abort_idx = c.exit_idx + 1;
     c.err_idx = c.abort_idx + 1;
-    c.total = c.err_idx + 4;
+    c.amax_idx = (c.err_idx + 4 + 1) & ~1;
+    c.total = c.amax_idx + 2 * n_seq;
     return c;
 }
 

@@ -108,7 +108,7 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_model_cfg *cfg, const mk_we
     // carve the fixed scratch
     const int32_t G = c.n_q_heads / c.n_kv_heads, S = g.attn_splits;
     const int32_t qkv_rows = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
-    const CtlLayout cl = ctl_layout(g.n_events, c.batch * c.n_kv_heads, 0);
+    const CtlLayout cl = ctl_layout(g.n_events, c.batch * c.n_kv_heads, 0, c.batch);
     Carve cv;
     const size_t o_layers = cv.take(sizeof(LayerW) * c.n_layers);
     const size_t o_tasks = cv.take(sizeof(Task) * t.tasks.size());

@@ -238,3 +238,36 @@ def test_tiny_ring_and_attention_step_options(cuda_device, opts):
     plan, kv = harness.gpu_plan(TINY, 256, opts=mk.mk_plan_options(**opts))
     model = harness.oracle_model(TINY)
     harness.run_teacher_forced(plan, kv, model, synth.tokens(150, 0, 9, TINY.vocab), 4, 256)
+
+
+@pytest.mark.parametrize("name,batch", [("tiny", 1), ("1b", 1), ("tiny", 4)], ids=["tiny-b1", "1b-b1", "tiny-b4"])
+def test_fused_greedy_step_matches_step_then_pick(cuda_device, name, batch):
+    """mk_decode_step_greedy (the pick fused into the decode launch at batch
+    1, a second launch when batched) gives the logits, tokens and positions
+    of mk_decode_step followed by mk_greedy_next, bit for bit."""
+    import torch
+
+    m = WORKLOADS[name].model
+    max_seq = 128
+    plan, kv_a = harness.gpu_plan(m, max_seq, batch=batch)
+    kv_b = mk.KVCache(m, batch, max_seq, shuffle_seed=1)
+    prompt = np.stack([synth.tokens(40, 0, b, m.vocab) for b in range(batch)])
+    logits_a = torch.empty((batch, m.vocab), dtype=torch.float32, device=cuda_device)
+    plan.prefill(torch.tensor(prompt, dtype=torch.int32, device=cuda_device), kv_a, logits_a)
+    plan.check()
+    kv_b.k.copy_(kv_a.k)
+    kv_b.v.copy_(kv_a.v)
+    kv_b.page_table.copy_(kv_a.page_table)
+    tok_a = torch.zeros(batch, dtype=torch.int32, device=cuda_device)
+    pos_a = torch.full((batch,), 39, dtype=torch.int32, device=cuda_device)
+    plan.greedy_next(logits_a, tok_a, pos_a)
+    tok_b, pos_b = tok_a.clone(), pos_a.clone()
+    logits_b = torch.empty_like(logits_a)
+    for step in range(4):
+        plan.decode_step(tok_a, pos_a, kv_a, logits_a)
+        plan.greedy_next(logits_a, tok_a, pos_a)
+        plan.decode_step_greedy(tok_b, pos_b, kv_b, logits_b)
+        plan.check()
+        assert torch.equal(logits_a, logits_b), f"step {step}: logits differ"
+        assert torch.equal(tok_a, tok_b) and torch.equal(pos_a, pos_b), f"step {step}: {tok_a} {tok_b} {pos_a} {pos_b}"
+        assert int(pos_b[0]) == 41 + step
