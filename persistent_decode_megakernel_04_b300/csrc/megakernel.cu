@@ -876,12 +876,21 @@ struct Consumer {
         const bool has_resid = (op == OP_O || op == OP_DOWN);
         const int32_t nrows = t.a1 - t.a0;
         const bool resid_in_smem = has_resid && nrows <= kMaxResid;
+        // residual rows of this task: loaded now into registers, stored to
+        // shared memory just before the barrier that precedes their first use
+        // (so that no warp waits for them at the task's start)
+        static_assert(kMaxResid % kComputeThreads == 0, "residual rows per thread");
+        float rv[kMaxResid / kComputeThreads];
+        bool resid_stored = !resid_in_smem;
         if (resid_in_smem) {
-            // residual rows of this task, read once up front (ordered by the first group's barrier)
-            for (int32_t i = ct; i < nrows; i += kComputeThreads)
-                c.sc->resid[i] = (op == OP_O && t.layer == 0)
-                                     ? __uint_as_float((uint32_t)p.embed[(int64_t)token * p.H + t.a0 + i] << 16)
-                                     : __ldcg(p.x + t.a0 + i);
+#pragma unroll
+            for (int k = 0; k < kMaxResid / kComputeThreads; ++k) {
+                const int32_t i = ct + k * kComputeThreads;
+                rv[k] = i >= nrows ? 0.f
+                                   : ((op == OP_O && t.layer == 0)
+                                          ? __uint_as_float((uint32_t)p.embed[(int64_t)token * p.H + t.a0 + i] << 16)
+                                          : __ldcg(p.x + t.a0 + i));
+            }
         }
 
         const uint16_t *emb_row = (op == OP_QKV && t.layer == 0) ? p.embed + (int64_t)token * p.H : nullptr;
@@ -890,18 +899,38 @@ struct Consumer {
             op == OP_QKV ? lw.attn_norm : (op == OP_GU ? lw.mlp_norm : (op == OP_LM ? p.final_norm : nullptr));
         const bool resident = g.ksplit <= kMvResident;
         float xr[kMvResident][8];
+        uint4 gr[kMvResident];  // RMSNorm gains of the resident chunks, loaded with the input
         float ss = 0.f;
+        if (resident || gain != nullptr) {
 #pragma unroll
-        for (int j = 0; j < kMvResident; ++j) {
-            load_piece(p, xin, emb_row, nullptr, 1.f, nchunk, j < g.ksplit ? j : 1 << 20, xr[j]);
+            for (int j = 0; j < kMvResident; ++j)
+                load_piece(p, xin, emb_row, nullptr, 1.f, nchunk, j < g.ksplit ? j : 1 << 20, xr[j]);
+            if (resident && gain != nullptr) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ss = fmaf(xr[j][e], xr[j][e], ss);
+                for (int j = 0; j < kMvResident; ++j) {
+                    const int32_t ch = ct + kComputeThreads * j;
+                    gr[j] = ch < nchunk ? __ldg(reinterpret_cast<const uint4 *>(gain) + ch) : make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kMvResident; ++j)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss = fmaf(xr[j][e], xr[j][e], ss);
         }
-        for (int j = kMvResident; j < g.ksplit; ++j) {
-            float v[8];
-            load_piece(p, xin, emb_row, nullptr, 1.f, nchunk, j, v);
+        if (gain != nullptr) {
+            // the rest of a streamed input, for the sum of squares only: four
+            // pieces' loads in flight at a time (a streamed input without a
+            // norm, the down projection's, skips this pass)
+            for (int j = kMvResident; j < g.ksplit; j += 4) {
+                float v[4][8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
+                for (int a = 0; a < 4; ++a)
+                    load_piece(p, xin, emb_row, nullptr, 1.f, nchunk, j + a < g.ksplit ? j + a : 1 << 20, v[a]);
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) ss = fmaf(v[a][e], v[a][e], ss);
+            }
         }
         float rn = 1.f;
         if (gain != nullptr) {
@@ -919,7 +948,7 @@ struct Consumer {
                 for (int j = 0; j < kMvResident; ++j) {
                     const int32_t ch = ct + kComputeThreads * j;
                     if (ch < nchunk) {
-                        const uint4 gv = __ldg(reinterpret_cast<const uint4 *>(gain) + ch);
+                        const uint4 gv = gr[j];
                         xr[j][0] *= rn * bf16_lo(gv.x); xr[j][1] *= rn * bf16_hi(gv.x);
                         xr[j][2] *= rn * bf16_lo(gv.y); xr[j][3] *= rn * bf16_hi(gv.y);
                         xr[j][4] *= rn * bf16_lo(gv.z); xr[j][5] *= rn * bf16_hi(gv.z);
@@ -1001,6 +1030,14 @@ struct Consumer {
             ++pg;
             row += n;
             if (pg == kPartGroups || row >= t.a1) {
+                if (!resid_stored) {
+#pragma unroll
+                    for (int k = 0; k < kMaxResid / kComputeThreads; ++k) {
+                        const int32_t i = ct + k * kComputeThreads;
+                        if (i < nrows) c.sc->resid[i] = rv[k];
+                    }
+                    resid_stored = true;
+                }
                 compute_bar();  // every warp's totals of the waiting groups are in
                 mv_finish(c, t, g, pg, resid_in_smem, out_qkv, out_x, out_h, out_logits, embed_row, best);
                 pg = 0;
