@@ -194,7 +194,10 @@ def run_reference(args, wl):
         "impl": "reference", "metric": METRIC, "value": ms, "unit": "ms/token", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded random-init weights)",
-        "config": {"workload": args.workload, "model": m.name, "batch": wl.batch, "prompt_len": wl.prompt_len},
+        "config": {"workload": args.workload, "model": m.name, "batch": wl.batch, "prompt_len": wl.prompt_len,
+                   "context": "seeded paged cache" if seeded_context(wl) else "prefilled prompt",
+                   "ctx_first_timed": wl.prompt_len + 1, "ctx_last_timed": wl.prompt_len + args.steps,
+                   "parallelism": "replicas x1"},
         "cpu_baseline": {"value": ms, "unit": "ms/token", "cores": threads, "kind": "oracle", "sample": desc},
         "e2e": {"value": ms, "unit": "ms/token", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
