@@ -204,6 +204,52 @@ def run_reference(args, wl):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------- ranks
+
+class Ranks:
+    """One process per GPU under torchrun (RANK, LOCAL_RANK and WORLD_SIZE
+    from the environment), or a single process.  Replicas only: no data
+    crosses ranks; the timed region is bracketed by barriers and its length
+    is the maximum over ranks."""
+
+    def __init__(self, backend: str, device=None):
+        import torch.distributed as dist
+
+        self.dist = dist
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.device = device
+        if self.world > 1:
+            if backend == "nccl":
+                dist.init_process_group(backend, device_id=device)
+            else:
+                dist.init_process_group(backend)
+
+    def barrier(self):
+        if self.world > 1:
+            self.dist.barrier()
+
+    def max(self, v: float) -> float:
+        if self.world == 1:
+            return v
+        import torch
+
+        t = torch.tensor([v], dtype=torch.float64, device=self.device)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.world > 1 and self.dist.is_initialized():
+            self.dist.destroy_process_group()
+
+
+def job_rates(ms_step_max: float, batch: int, world: int):
+    """(ms per token of each replica, whole-job tokens/s) from the slowest
+    rank's ms per step; every rank decodes `batch` sequences per step."""
+    return ms_step_max / batch, 1e3 / ms_step_max * batch * world
+
+
 # ----------------------------------------------------------------- GPU side
 
 def seeded_context(wl) -> bool:
@@ -214,17 +260,14 @@ def seeded_context(wl) -> bool:
 
 def run_mk(args, wl):
     import torch
-    import torch.distributed as dist
 
     import persistent_decode_megakernel_04_b300 as mk
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=dev)
+    ranks = Ranks("nccl", dev)
+    world, rank = ranks.world, ranks.rank
     m = wl.model
     B = wl.batch
     max_seq = ((wl.prompt_len + args.warmup + args.steps + args.e2e_steps + 4 + 63) // 64) * 64
@@ -302,8 +345,7 @@ def run_mk(args, wl):
             g_step = g_pick = None
             torch.cuda.synchronize()
             plan.check()
-    if world > 1:
-        dist.barrier()
+    ranks.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         time.sleep(0.3)
@@ -321,15 +363,11 @@ def run_mk(args, wl):
                 step_pick()
         end.record(stream)
         torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
+    ranks.barrier()
     plan.check()
-    ms_step = start.elapsed_time(end) / args.steps
+    ms_step = ranks.max(start.elapsed_time(end) / args.steps)
     kern_ms = [a.elapsed_time(b) for a, b in ev]
-    if world > 1:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_token, tokens_per_s = job_rates(ms_step, B, world)
     bytes_total = sum(step_bytes(m, B, ctx0 + i) for i in range(args.steps))
     achieved = bytes_total / (sum(kern_ms) / 1e3) / 1e9
     peak, peak_src = measured_peak()
@@ -402,7 +440,7 @@ def run_mk(args, wl):
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": ms_step / B, "unit": "ms/token", "n_gpus": world, "steps": args.steps,
+            "metric": METRIC, "value": ms_token, "unit": "ms/token", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16 weights/KV, fp32 math",
             "data": "synthetic (seeded random-init weights, random prompt ids)",
@@ -414,7 +452,7 @@ def run_mk(args, wl):
                        "greedy_pick": "in the decode launch" if fused else "separate kernel",
                        **({"plan_options": kw} if kw else {}),
                        "l2": f"no flush: {weight_bytes_read(m, B) / 1e9:.1f} GB of weights stream per step (> 126 MB L2)"},
-            "tokens_per_s": 1e3 / ms_step * B * world,
+            "tokens_per_s": tokens_per_s,
             "hbm_gbs": achieved,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_src,
@@ -430,8 +468,7 @@ def run_mk(args, wl):
         }
         print(json.dumps(line), flush=True)
     plan.close()
-    if world > 1:
-        dist.destroy_process_group()
+    ranks.close()
 
 
 def main():

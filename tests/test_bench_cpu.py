@@ -40,3 +40,57 @@ def test_reference_arm_other_ranks_do_no_work():
     r = _run({"RANK": "1", "WORLD_SIZE": "2"})
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip() == ""
+
+
+def _free_port() -> int:
+    import socket
+
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _replica_rank(rank: int, world: int, port: int, out_dir: str):
+    """One bench rank on the CPU (gloo): barriers around a 'timed region' whose
+    length differs per rank, then the maximum over ranks."""
+    os.environ.update({"RANK": str(rank), "LOCAL_RANK": str(rank), "WORLD_SIZE": str(world),
+                       "MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
+    sys.path.insert(0, str(ROOT))
+    import bench
+
+    ranks = bench.Ranks("gloo")
+    assert (ranks.world, ranks.rank) == (world, rank)
+    ranks.barrier()
+    ms_step = 3.0 + rank  # rank r "took" 3 + r ms per step
+    ms_max = ranks.max(ms_step)
+    ranks.barrier()
+    ms_token, tok_s = bench.job_rates(ms_max, 4, world)
+    Path(out_dir, f"rank{rank}.json").write_text(json.dumps([ms_max, ms_token, tok_s]))
+    ranks.close()
+
+
+def test_two_replica_ranks_take_the_slowest_rank_on_gloo(tmp_path):
+    import torch.multiprocessing as tmp
+
+    world = 2
+    tmp.spawn(_replica_rank, args=(world, _free_port(), str(tmp_path)), nprocs=world, join=True)
+    got = [json.loads((tmp_path / f"rank{r}.json").read_text()) for r in range(world)]
+    for ms_max, ms_token, tok_s in got:
+        assert ms_max == 4.0  # the slower rank's time, seen by every rank
+        assert ms_token == 1.0  # 4 sequences per step on each replica
+        assert abs(tok_s - 1e3 / 4.0 * 4 * world) < 1e-9  # both replicas' tokens
+
+
+def test_single_process_ranks_need_no_process_group():
+    sys.path.insert(0, str(ROOT))
+    import bench
+
+    env = {k: os.environ.pop(k) for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK") if k in os.environ}
+    try:
+        r = bench.Ranks("gloo")
+        assert (r.world, r.rank) == (1, 0)
+        r.barrier()
+        assert r.max(2.5) == 2.5
+        r.close()
+    finally:
+        os.environ.update(env)
