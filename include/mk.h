@@ -102,7 +102,7 @@ typedef struct {
     int32_t attn_splits;   /* context splits per (sequence, kv head), at most 64
                               (default: CTAs / (batch*n_kv_heads), capped at 64) */
     int32_t slot_bytes;    /* shared-memory ring slot size (default 32768) */
-    int32_t num_slots;     /* ring slots (default 6) */
+    int32_t num_slots;     /* ring slots (default 6 at batch 1; batched: as many as shared memory holds) */
     int32_t timeout_ms;    /* budget of every device wait (default 2000) */
     uint32_t planner_seed; /* nonzero: permute the CTA <-> tile assignment */
     int32_t l2_prefetch_kb;/* batch 1: on reaching an O projection, prefetch into L2 up to this many
