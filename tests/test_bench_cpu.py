@@ -94,3 +94,33 @@ def test_single_process_ranks_need_no_process_group():
         r.close()
     finally:
         os.environ.update(env)
+
+
+def _hand_weight_bytes(L, H, nq, nkv, d, I, V, batch):
+    """bf16 bytes of one step's weights, written out from the decoder's
+    matrices: Wq, Wo (nq*d x H), Wk, Wv (nkv*d x H), gate, up, down (I x H),
+    two norm gains per layer; the LM head, the final gain, one embedding row
+    per sequence."""
+    per_layer = 2 * nq * d * H + 2 * nkv * d * H + 3 * I * H + 2 * H
+    return 2 * (L * per_layer + V * H + H + batch * H)
+
+
+def test_algorithmic_bytes_match_the_shapes():
+    sys.path.insert(0, str(ROOT))
+    import bench
+    from synth import WORKLOADS
+
+    m8 = WORKLOADS["8b"].model
+    assert bench.weight_bytes_read(m8, 1) == _hand_weight_bytes(32, 4096, 32, 8, 128, 14336, 128256, 1)
+    assert bench.weight_bytes_read(m8, 1) == 15_009_857_536  # 15.010 GB, 436.2 MB per layer
+    m1 = WORKLOADS["1b"].model
+    assert bench.weight_bytes_read(m1, 1) == _hand_weight_bytes(16, 2048, 32, 8, 64, 8192, 128256, 1)
+    assert bench.weight_bytes_read(m1, 1) == 2_471_632_896  # 2.4716 GB (tied: the LM head is the embedding)
+    m70 = WORKLOADS["70b"].model
+    assert bench.weight_bytes_read(m70, 16) == _hand_weight_bytes(80, 8192, 64, 8, 128, 28672, 128256, 16)
+    # K and V of one cached token over every layer: 128 KB (8B), 32 KB (1B), 320 KB (70B)
+    for m, per_tok in ((m8, 131072), (m1, 32768), (m70, 327680)):
+        for B in (1, 8):
+            assert bench.step_bytes(m, B, 101) - bench.step_bytes(m, B, 100) == B * per_tok
+        # a step at context 1 (empty cache) writes the new K/V and the fp32 logits only
+        assert bench.step_bytes(m, 2, 1) == bench.weight_bytes_read(m, 2) + 2 * (per_tok + m.vocab * 4)
