@@ -178,7 +178,7 @@ def oracle_sample(m, steps: int, pos0: int, seed: int = 0, n_layers_gen: int = 2
         model.head(x)
         times.append(time.perf_counter() - t0)
     per_token_ms = 1e3 * statistics.mean(times) * m.n_layers
-    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    threads = oracle.num_threads()
     desc = (f"{steps} samples of one {m.name} decoder layer + 1/{m.n_layers} of the LM-head rows at positions "
             f"{pos0}..{pos0 + steps - 1}, fp64 oracle, scaled x{m.n_layers} to one token")
     return per_token_ms, threads, desc

@@ -66,6 +66,8 @@ def lib():
     if _lib is None:
         build()
         L = ctypes.CDLL(str(LIB_PATH))
+        L.orc_num_threads.restype = _i
+        L.orc_num_threads.argtypes = []
         L.orc_bf16.restype = _d
         L.orc_bf16.argtypes = [ctypes.c_uint16]
         L.orc_rmsnorm.argtypes = [_i, _p, _p, _d, _p]
@@ -81,6 +83,11 @@ def lib():
         L.orc_full_forward.argtypes = [_p, _p, _i, _p, _p]
         _lib = L
     return _lib
+
+
+def num_threads() -> int:
+    """Threads the oracle's parallel loops run with in this process."""
+    return int(lib().orc_num_threads())
 
 
 def _f64(a) -> np.ndarray:

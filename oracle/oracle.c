@@ -28,6 +28,7 @@
  * rows across threads; it never changes an individual sum.
  */
 #include <math.h>
+#include <omp.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -56,6 +57,18 @@ typedef struct {
     const uint16_t *final_norm; /* [hidden] */
     const orc_layer_w *layers;  /* [n_layers] */
 } orc_weights;
+
+/* Threads of the team that a parallel loop of this library runs with (what
+ * a timed run of the oracle actually used; no arithmetic). */
+int orc_num_threads(void) {
+    int n = 1;
+#pragma omp parallel
+    {
+#pragma omp single
+        n = omp_get_num_threads();
+    }
+    return n;
+}
 
 double orc_bf16(uint16_t h) {
     uint32_t u = (uint32_t)h << 16;

@@ -124,3 +124,10 @@ def test_algorithmic_bytes_match_the_shapes():
             assert bench.step_bytes(m, B, 101) - bench.step_bytes(m, B, 100) == B * per_tok
         # a step at context 1 (empty cache) writes the new K/V and the fp32 logits only
         assert bench.step_bytes(m, 2, 1) == bench.weight_bytes_read(m, 2) + 2 * (per_tok + m.vocab * 4)
+
+
+def test_cpu_baseline_reports_the_threads_the_oracle_ran_with():
+    r = _run({"OMP_NUM_THREADS": "2"})
+    assert r.returncode == 0, r.stderr
+    d = json.loads([l for l in r.stdout.splitlines() if l.strip()][-1])
+    assert d["cpu_baseline"]["cores"] == 2
