@@ -129,8 +129,11 @@ typedef struct {
     int32_t detail; /* event id, task index or offending value */
 } mk_device_error;
 
-/* Build a plan for one decoder and batch geometry on the current device:
- * validates the shape and pointer alignment, builds the task graph (per-CTA
+/* Build a plan for one decoder and batch geometry on the current device.
+ * Passage: the ahead-of-time task graph of "MPK: A Compiler and Runtime for
+ * Mega-Kernelizing Tensor Programs", sections 2-3 (tGraph, AOT preparation),
+ * and "Compilar LLM en un MegaKernel…", "Parte 1. Compilador".
+ * Validates the shape and pointer alignment, builds the task graph (per-CTA
  * task queues and event thresholds), allocates the plan's scratch and
  * checks that the cooperative grid fits.  Synchronous.  *out is set only on
  * MK_OK.  MK_ERR_UNSUPPORTED: a shape this build does not implement. */
@@ -138,37 +141,52 @@ mk_status mk_plan_create(const mk_model_cfg *cfg, const mk_weight_ptrs *w, mk_pl
 mk_status mk_plan_create_ex(const mk_model_cfg *cfg, const mk_weight_ptrs *w, const mk_plan_options *opt,
                             mk_plan **out);
 
-/* One decode step for every sequence of the batch: tokens[b] at position
+/* One decode step for every sequence of the batch.  Passage: the single
+ * persistent launch of "Compilar LLM en un MegaKernel…", sections "Parte 2.
+ * Runtime" and "Método de ejecución basado en eventos"; the fused task list
+ * of "Llama-70B 向け…megakernel", section 高スループットMegakernelの設計と工夫.
+ * tokens[b] at position
  * positions[b] (device int32 [batch]).  Appends K/V of that position to the
  * cache, attends over positions 0..positions[b], writes logits (device fp32
  * [batch][vocab]).  One cooperative launch. */
 mk_status mk_decode_step(mk_plan *plan, const int32_t *tokens, const int32_t *positions, const mk_kv_cache *kv,
                          float *logits, void *stream);
 
-/* The same step, with the same task code, launched one kernel per operator
+/* Passage: the separate-kernel baseline that "Compilar LLM en un
+ * MegaKernel…" compares against ("Limitaciones previas"), and the
+ * measurement checklist of "Cómo la fusión de kernels CUDA acelera…",
+ * "Comprueba si la fusión ha ayudado".
+ * The same step, with the same task code, launched one kernel per operator
  * and layer (5 per layer + 1), ordered by the stream instead of by event
  * counters.  The launch-per-operator ablation of the megakernel. */
 mk_status mk_decode_step_ablation(mk_plan *plan, const int32_t *tokens, const int32_t *positions,
                                   const mk_kv_cache *kv, float *logits, void *stream);
 
-/* mk_decode_step with HOST buffers: copies tokens/positions (host int32
+/* Passage: as mk_decode_step (a serving loop's view of one step).
+ * mk_decode_step with HOST buffers: copies tokens/positions (host int32
  * [batch]) in, runs the step, copies logits (host fp32 [batch][vocab]) out
  * and synchronises `stream`.  Returns device errors of this step directly. */
 mk_status mk_decode_step_host(mk_plan *plan, const int32_t *tokens_host, const int32_t *positions_host,
                               const mk_kv_cache *kv, float *logits_host, void *stream);
 
-/* Prefill T prompt tokens per sequence (device int32 [batch][T]) at
+/* Passage: the prompt phase before decoding ("Compilar LLM en un
+ * MegaKernel…", "Valor central de MPK": a 39-token prompt, then 512 decode
+ * steps).
+ * Prefill T prompt tokens per sequence (device int32 [batch][T]) at
  * positions 0..T-1 by running the decode step once per position; writes the
  * logits of position T-1 (device fp32 [batch][vocab]).  The LM head runs only
  * for the last position. */
 mk_status mk_prefill(mk_plan *plan, const int32_t *tokens, int32_t T, const mk_kv_cache *kv, float *last_logits,
                      void *stream);
 
-/* Greedy continuation for the next step: tokens[b] = argmax_v logits[b][v]
+/* Passage: greedy decoding of the measured runs ("Valor central de MPK").
+ * Greedy continuation for the next step: tokens[b] = argmax_v logits[b][v]
  * (lowest index on ties) and positions[b] += 1, on the device. */
 mk_status mk_greedy_next(mk_plan *plan, const float *logits, int32_t *tokens, int32_t *positions, void *stream);
 
-/* One decode step followed by the greedy pick, in place: tokens[b] becomes
+/* Passage: the fused LM-head epilogue of "Cómo la fusión de kernels CUDA
+ * acelera…", section "Sigue los datos intermedios".
+ * One decode step followed by the greedy pick, in place: tokens[b] becomes
  * the argmax of row b of logits (the lowest index among equal maxima; NaN
  * never wins, and a row without a finite maximum gives 0x7FFFFFFF) and
  * positions[b] is incremented, exactly as mk_decode_step then
@@ -180,7 +198,10 @@ mk_status mk_greedy_next(mk_plan *plan, const float *logits, int32_t *tokens, in
 mk_status mk_decode_step_greedy(mk_plan *plan, int32_t *tokens, int32_t *positions, const mk_kv_cache *kv,
                                 float *logits, void *stream);
 
-/* Task trace of the last step run with a plan created with options.trace:
+/* Passage: the 1-2 us task-switch cost that "Compilar LLM en un
+ * MegaKernel…" reports ("Método de ejecución basado en eventos"); this call
+ * measures it.
+ * Task trace of the last step run with a plan created with options.trace:
  * for every CTA c and queue position i (the order of mk_plan_describe),
  * out[(c * *max_tasks + i) * 8 + k] holds, in globaltimer nanoseconds,
  *   k=0 scheduler released the task (its event reached the threshold),
@@ -203,12 +224,12 @@ mk_status mk_plan_trace(mk_plan *plan, void *stream, uint64_t *out, int64_t capa
  *
  * The pages have no counterpart to this call. It exists for callers that
  * cannot call cudaMalloc when they need a decode step: code running while a
- * memory pool or a CUDA graph owns the device's allocations, a runtime that
- * reserves all device memory up front, or a serving process that must not
- * grow its footprint. It needs no plan. Each call builds the task graph on
- * the host from `cfg` (batch must be 1; other values return
- * MK_ERR_UNSUPPORTED), then runs the same persistent kernel as
- * mk_decode_step, with the same arguments and results.
+ * caching allocator or memory pool holds all of the device's free memory, a
+ * runtime that reserves all device memory up front, or a serving process
+ * that must not grow its footprint once it is serving. It needs no plan.
+ * Each call builds the task graph on the host from `cfg` (batch must be 1;
+ * other values return MK_ERR_UNSUPPORTED), then runs the same persistent
+ * kernel as mk_decode_step, with the same arguments and results.
  *
  * Scratch: every call uses one fixed 16 MiB device array, compiled into this
  * library. Every GPU that loads the library holds those 16 MiB until the
@@ -219,24 +240,33 @@ mk_status mk_plan_trace(mk_plan *plan, void *stream, uint64_t *out, int64_t capa
  * the launch. Calls that overlap on the GPU (on two streams at once) share the
  * array and race: issue them one at a time.
  *
- * The first call on a device looks up the array's device address on that
- * device (cudaGetSymbolAddress). Make that first call before any stream
- * capture. The call calls no cudaMalloc or cudaFree.
+ * The first call on a device (and the first after the device's context has
+ * been replaced, for example by cudaDeviceReset) looks up the array's device
+ * address on that device with cudaGetSymbolAddress. Make that first call
+ * before any stream capture. The call calls no cudaMalloc or cudaFree.
  *
- * The call is synchronous: it synchronises `stream` and returns the step's
- * device-detected error (MK_ERR_BOUNDS, MK_ERR_TIMEOUT), if any, as its
- * status. weights, tokens, positions, kv and logits are as for
+ * The call is synchronous: it waits for `stream` before it returns, and
+ * returns the step's device-detected error (MK_ERR_BOUNDS, MK_ERR_TIMEOUT), if
+ * any, as its status. weights, tokens, positions, kv and logits are as for
  * mk_plan_create and mk_decode_step. */
 mk_status mk_decode_step_noalloc(const mk_model_cfg *cfg, const mk_weight_ptrs *w, const int32_t *tokens,
                                  const int32_t *positions, const mk_kv_cache *kv, float *logits, void *stream);
 
-/* Synchronises `stream`, reads and clears the plan's device error word. */
+/* Passage: none on the pages (error reporting of this library).
+ * Synchronises `stream`, reads and clears the plan's device error word, and
+ * returns the status it held.  It takes the stream the plan's steps run on
+ * and an optional report (info, may be NULL) beyond the plain
+ * mk_plan_last_error(plan) form: the stream says which work to wait for, and
+ * the report names the site, CTA and offending value.  The read is one
+ * copy on `stream` into host memory, then one synchronisation; clearing, when
+ * an error was set, resets every control word of the plan. */
 mk_status mk_plan_last_error(mk_plan *plan, void *stream, mk_device_error *info);
 
 const char *mk_status_string(mk_status s);
 const char *mk_error_site_string(int32_t site);
 
-/* Frees the plan's device memory.  Synchronises the device first. */
+/* Passage: none on the pages.  Frees the plan's device memory.
+ * Synchronises the device first. */
 void mk_plan_destroy(mk_plan *plan);
 
 /* ---------------------------------------------------------------------
@@ -256,7 +286,9 @@ typedef struct {
     int32_t a2, a3;      /* attention: split index, number of splits; projections: range number a2 */
 } mk_task_info;
 
-/* Builds the task graph for `num_ctas` worker CTAs without touching a GPU.
+/* Passage: the task graph of "Compilar LLM en un MegaKernel…", "Parte 1.
+ * Compilador" (tasks, events, dependencies), as a host-only listing.
+ * Builds the task graph for `num_ctas` worker CTAs without touching a GPU.
  * Writes up to `capacity` tasks (queue order, CTA by CTA) to out, the task
  * count to *n_tasks and the number of event counters to *n_events.
  * MK_ERR_INVALID if capacity is too small (n_tasks still set). */

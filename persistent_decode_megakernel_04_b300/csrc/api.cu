@@ -36,6 +36,7 @@ struct mk_plan {
     int32_t *d_stage_tok = nullptr;  // staging for the host-buffer entry point
     int32_t *d_stage_pos = nullptr;
     float *d_stage_logits = nullptr;
+    uint32_t *h_err = nullptr;       // pinned host copy of the device error word
     uint64_t *d_trace = nullptr;
     int32_t trace_stride = 0;
     // batched path
@@ -148,6 +149,7 @@ mk_status cuda_status(cudaError_t e) {
 }
 
 void free_plan(mk_plan *p) {
+    if (p->h_err) cudaFreeHost(p->h_err);
     for (void *q : p->allocs) cudaFree(q);
     p->allocs.clear();
     delete p;
@@ -320,6 +322,13 @@ mk_status mk_plan_create_ex(const mk_model_cfg *cfg, const mk_weight_ptrs *w, co
         (st = dev_alloc(p, &p->d_stage_logits, (size_t)c.batch * c.vocab))) {
         free_plan(p);
         return st;
+    }
+    if (cudaHostAlloc(reinterpret_cast<void **>(&p->h_err), 4 * sizeof(uint32_t), cudaHostAllocDefault) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        p->h_err = nullptr;
+        free_plan(p);
+        return MK_ERR_OOM;
     }
     const int32_t n_tmaps = c.n_layers * 7 + 4;
     if (g.tc) {
@@ -547,15 +556,17 @@ mk_status mk_greedy_next(mk_plan *p, const float *logits, int32_t *tokens, int32
 mk_status mk_plan_last_error(mk_plan *p, void *stream, mk_device_error *info) {
     if (!p) return MK_ERR_INVALID;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    uint32_t words[4] = {0, 0, 0, 0};
-    cudaError_t e = cudaStreamSynchronize(s);
-    if (e == cudaSuccess)
-        e = cudaMemcpy(words, p->d_ctl + p->cl.err_idx, sizeof(words), cudaMemcpyDeviceToHost);
+    // one copy on the plan's stream into pinned memory, then one wait
+    cudaError_t e = cudaMemcpyAsync(p->h_err, p->d_ctl + p->cl.err_idx, 4 * sizeof(uint32_t),
+                                    cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_status(e);
+    uint32_t words[4];
+    std::memcpy(words, p->h_err, sizeof(words));
     if (words[0] != 0) {
         // clear the error, the abort flag and every counter for the next launch
-        e = cudaMemset(p->d_ctl, 0, (size_t)p->cl.total * sizeof(uint32_t));
-        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+        e = cudaMemsetAsync(p->d_ctl, 0, (size_t)p->cl.total * sizeof(uint32_t), s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
         if (e != cudaSuccess) return cuda_status(e);
     }
     if (info) {

@@ -38,6 +38,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
 #include <type_traits>
 
 #include "mk_kernel.h"
@@ -1993,6 +1994,15 @@ int megakernel_variant(int32_t /*max_k*/, bool /*tc*/) {
 }
 
 cudaError_t megakernel_set_smem(int variant, size_t smem) {
+    // The dynamic shared-memory limit belongs to the kernel function, so every
+    // plan and call in the process shares it: only ever raise it, or a plan
+    // made earlier with a larger ring could no longer launch.
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lk(mu);
+    cudaFuncAttributes a{};
+    cudaError_t e = cudaFuncGetAttributes(&a, variant_ptr(variant));
+    if (e != cudaSuccess) return e;
+    if ((size_t)a.maxDynamicSharedSizeBytes >= smem) return cudaSuccess;
     return cudaFuncSetAttribute(variant_ptr(variant), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
 }
 

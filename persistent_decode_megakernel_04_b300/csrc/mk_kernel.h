@@ -101,6 +101,8 @@ int megakernel_variant(int32_t max_k, bool tc);
 cudaError_t launch_megakernel(const KParams &p, int variant, int grid, size_t smem, bool cooperative,
                               cudaStream_t stream);
 cudaError_t megakernel_max_active(int variant, size_t smem, int *blocks_per_sm);
+// Raises the kernel's dynamic shared-memory limit to at least smem (never
+// lowers it: the limit is shared by every plan and call in the process).
 cudaError_t megakernel_set_smem(int variant, size_t smem);
 
 // Host: TMA maps of the K and V pools (KParams::kv_maps) for tiles of ts tokens.

@@ -10,6 +10,8 @@
 // counters and error word) lives in one file-scope __device__ array of
 // kNoAllocScratchBytes. The caller passes inputs and outputs, as for
 // mk_decode_step.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -32,25 +34,66 @@ constexpr size_t kNoAllocScratchBytes = 16u << 20;  // 16 MiB
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 // In host code, g_noalloc_scratch names a host-side stand-in, not a device
-// address. Its device address is looked up once per device, with that device
-// current, and cached here.
+// address. Its device address is looked up with the device current, once per
+// device and CUDA context, and cached here. The context's unique id is kept
+// beside it: after cudaDeviceReset the device gets a new primary context, in
+// which the array may sit elsewhere, and the address is looked up again.
 constexpr int kMaxDevices = 64;
-void *g_scratch_dev[kMaxDevices] = {};
+struct ScratchAddr {
+    unsigned long long ctx_id = 0;
+    void *ptr = nullptr;
+};
+ScratchAddr g_scratch_dev[kMaxDevices];
 std::mutex g_scratch_mu;
 
+// Unique id of the calling thread's current CUDA context (driver entry
+// points, looked up once; no libcuda link).
+bool current_context_id(unsigned long long *id) {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    if (!get_current || !get_id) {
+        void *f = nullptr, *g = nullptr;
+        cudaDriverEntryPointQueryResult q1, q2;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q1) != cudaSuccess ||
+            q1 != cudaDriverEntryPointSuccess ||
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &g, 12000, cudaEnableDefault, &q2) != cudaSuccess ||
+            q2 != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+        get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(g);
+    }
+    CUcontext ctx = nullptr;
+    unsigned long long v = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr || get_id(ctx, &v) != CUDA_SUCCESS) return false;
+    *id = v;
+    return true;
+}
+
+// Device address of the fixed scratch on `dev`, which must be current.
 mk_status scratch_address(int dev, unsigned char **out) {
     if (dev < 0 || dev >= kMaxDevices) return MK_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (!g_scratch_dev[dev]) {
+    // makes the device's primary context current (created if need be)
+    if (cudaSetDevice(dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MK_ERR_CUDA;
+    }
+    unsigned long long id = 0;
+    if (!current_context_id(&id)) return MK_ERR_CUDA;
+    ScratchAddr &a = g_scratch_dev[dev];
+    if (!a.ptr || a.ctx_id != id) {
         void *ptr = nullptr;
         const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
         if (e != cudaSuccess || !ptr) {
             cudaGetLastError();
             return MK_ERR_CUDA;
         }
-        g_scratch_dev[dev] = ptr;
+        a.ptr = ptr;
+        a.ctx_id = id;
     }
-    *out = static_cast<unsigned char *>(g_scratch_dev[dev]);
+    *out = static_cast<unsigned char *>(a.ptr);
     return MK_OK;
 }
 

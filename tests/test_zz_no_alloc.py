@@ -76,3 +76,37 @@ def test_noalloc_rejects_batched_and_oversized_shapes(cuda_device):
     big_kv = mk.mk_kv_cache(kv.desc.k_pool, kv.desc.v_pool, kv.desc.page_table, kv.desc.num_pages, (1 << 20) // 64)
     assert mk.lib().mk_decode_step_noalloc(ctypes.byref(huge), ctypes.byref(plan.wp), t.data_ptr(), t.data_ptr(),
                                            ctypes.byref(big_kv), logits.data_ptr(), None) == mk.MK_ERR_OOM
+
+
+def test_noalloc_call_keeps_a_larger_plan_launchable(cuda_device):
+    """The kernel's dynamic shared-memory limit is shared by every plan and
+    call in the process.  A plan made with a larger ring than the
+    allocation-free call uses must still launch after that call."""
+    import torch
+
+    m = WORKLOADS["tiny"].model
+    max_seq = 128
+    big, kv = harness.gpu_plan(m, max_seq, opts=mk.mk_plan_options(slot_bytes=33792))
+    model = harness.oracle_model(m)
+    prompt = synth.tokens(20, 0, 12, m.vocab)
+    kc, vc = model.new_cache(max_seq)
+    ref = model.prefill(kc, vc, prompt)
+    logits = torch.empty((1, m.vocab), dtype=torch.float32, device=cuda_device)
+    big.prefill(torch.tensor(prompt, dtype=torch.int32, device=cuda_device).view(1, -1), kv, logits)
+    big.check()
+    harness.compare_logits(logits.cpu().numpy()[0], ref, "larger-ring plan before the no-alloc call")
+    # the allocation-free call (default ring, less shared memory), on a cache of its own
+    kv_na = mk.KVCache(m, 1, max_seq, shuffle_seed=1)
+    t = torch.tensor([int(np.argmax(ref))], dtype=torch.int32, device=cuda_device)
+    p0 = torch.tensor([0], dtype=torch.int32, device=cuda_device)
+    out = torch.empty_like(logits)
+    st = mk.lib().mk_decode_step_noalloc(ctypes.byref(big.cfg), ctypes.byref(big.wp), t.data_ptr(), p0.data_ptr(),
+                                        ctypes.byref(kv_na.desc), out.data_ptr(),
+                                        torch.cuda.current_stream().cuda_stream)
+    assert st == mk.MK_OK, mk.mk_status_string(st)
+    # the larger plan's next step still launches and still matches the oracle
+    nxt = int(np.argmax(ref))
+    ref = model.decode_step(kc, vc, nxt, len(prompt))
+    big.decode_step(t, torch.tensor([len(prompt)], dtype=torch.int32, device=cuda_device), kv, logits)
+    big.check()
+    harness.compare_logits(logits.cpu().numpy()[0], ref, "larger-ring plan after the no-alloc call")
