@@ -438,6 +438,7 @@ def run_mk(args, wl):
         rows = mktrace.phases(tasks, tr)
         Path(args.trace_out).write_text(json.dumps(rows, indent=1))
         Path(args.trace_out).with_suffix(".chrome.json").write_text(mktrace.chrome_trace(tasks, tr))
+        np.save(Path(args.trace_out).with_suffix(".raw.npy"), tr)  # [cta][queue position][8] stamps
         tplan.close()
 
     cpu = None

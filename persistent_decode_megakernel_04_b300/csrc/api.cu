@@ -43,6 +43,7 @@ struct mk_plan {
     uint16_t *d_xa = nullptr, *d_attn_a = nullptr, *d_h_a = nullptr;
     float *d_ssq = nullptr, *d_tc_part = nullptr;
     uint8_t *d_tmaps = nullptr;
+    uint8_t *d_down_maps = nullptr;  // batch 1: per-layer w_down tensor maps
     KParams base{};
     // tensor maps of the last KV cache seen (encoded once per cache, not per step)
     mk_kv_cache kv_seen{};
@@ -90,6 +91,27 @@ bool encode_kv_maps(KParams &k, const mk_model_cfg &c, const mk_kv_cache &kv, in
     if (rows >= (1ull << 31)) return false;
     return encode_bf16_2d(reinterpret_cast<CUtensorMap *>(k.kv_maps[0]), kv.k_pool, c.head_dim, rows, ts) &&
            encode_bf16_2d(reinterpret_cast<CUtensorMap *>(k.kv_maps[1]), kv.v_pool, c.head_dim, rows, ts);
+}
+
+bool down_tma_ok(const MvGeom &g) {
+    return g.rps == 0 && g.row_mult == 1 && g.kc == 2048 && g.K % g.kc == 0 && g.ksplit > 2 && g.rpp >= 1 &&
+           g.rpp <= 8;
+}
+
+// w_down [rows][K] bf16 seen as [rows][K/256][256]: a box of rpp rows x
+// kc/256 blocks x 256 columns lands in shared memory as rpp rows of kc
+// columns, row r at byte offset r * kc * 2 (the bulk copies' slot layout).
+// Rows past the end read as zero.
+bool encode_down_map(void *m, const void *w_down, const MvGeom &g) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc || !down_tma_ok(g)) return false;
+    const cuuint64_t dims[3] = {256, (cuuint64_t)g.K / 256, (cuuint64_t)g.rows};
+    const cuuint64_t strides[2] = {512, (cuuint64_t)g.K * 2};
+    const cuuint32_t box[3] = {256, (cuuint32_t)g.kc / 256, (cuuint32_t)g.rpp};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return enc(reinterpret_cast<CUtensorMap *>(m), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(w_down),
+               dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace mk
@@ -343,6 +365,24 @@ mk_status mk_plan_create_ex(const mk_model_cfg *cfg, const mk_weight_ptrs *w, co
             return st;
         }
     }
+    if (!g.tc && down_tma_ok(g.mv[OP_DOWN])) {
+        // one TMA copy per down-projection slot instead of one bulk copy per row
+        std::vector<CUtensorMap> dm(c.n_layers);
+        bool ok = true;
+        for (int l = 0; l < c.n_layers && ok; ++l) ok = encode_down_map(&dm[l], w->w_down[l], g.mv[OP_DOWN]);
+        if (ok) {
+            if ((st = dev_alloc(p, &p->d_down_maps, dm.size() * sizeof(CUtensorMap))) != MK_OK) {
+                free_plan(p);
+                return st;
+            }
+            if (cudaMemcpy(p->d_down_maps, dm.data(), dm.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice) !=
+                cudaSuccess) {
+                cudaGetLastError();
+                free_plan(p);
+                return MK_ERR_CUDA;
+            }
+        }
+    }
     if (p->opt.trace) {
         for (int32_t i = 0; i < g.num_ctas; ++i)
             p->trace_stride = std::max(p->trace_stride, p->tables.queue_off[i + 1] - p->tables.queue_off[i]);
@@ -445,6 +485,7 @@ mk_status mk_plan_create_ex(const mk_model_cfg *cfg, const mk_weight_ptrs *w, co
     k.attn_splits = g.attn_splits;
     k.l2_prefetch_bytes = g.l2_prefetch_bytes;
     k.max_inflight = g.max_inflight;
+    k.down_maps = p->d_down_maps;
     k.only_op = -1;
     k.only_layer = -1;
     k.skip_lm = 0;

@@ -351,6 +351,19 @@ struct Producer {
         return true;
     }
 
+    // Starts ring slot number `issued`, which will receive `bytes` bytes:
+    // waits for a free slot (and the in-flight cap) and arms its full
+    // barrier.  False on abort or timeout.
+    __device__ __forceinline__ bool begin_slot(const Ctx &c, uint32_t *slot, uint32_t bytes) {
+        if (!acquire_slot(c, slot)) return false;
+        mbar_arrive_expect_tx(&c.sc->full[*slot], bytes);
+        return true;
+    }
+    // One contiguous piece of a slot.
+    __device__ __forceinline__ void copy(const Ctx &c, uint32_t s, uint8_t *dst, const void *src, uint32_t bytes) {
+        bulk_g2s(dst, src, bytes, &c.sc->full[s], pol);
+    }
+
     __device__ bool run_matvec(const Ctx &c, const Task &t) {
         const KParams &p = *c.p;
         const int op = t.op;
@@ -365,12 +378,11 @@ struct Producer {
             if (g.rps == 8 && g.row_mult == 2) {
                 // gate rows and up rows of the group in one slot: two contiguous copies
                 uint32_t s;
-                if (!acquire_slot(c, &s)) return false;
                 const uint32_t bytes = (uint32_t)(n * g.K * 2);
-                mbar_arrive_expect_tx(&c.sc->full[s], 2 * bytes);
+                if (!begin_slot(c, &s, 2 * bytes)) return false;
                 uint8_t *dst = c.ring + (size_t)s * slot_bytes;
-                bulk_g2s(dst, W + (int64_t)lr * g.K, bytes, &c.sc->full[s], pol);
-                bulk_g2s(dst + (size_t)4 * g.K * 2, lw.w_up + (int64_t)lr * g.K, bytes, &c.sc->full[s], pol);
+                copy(c, s, dst, W + (int64_t)lr * g.K, bytes);
+                copy(c, s, dst + (size_t)4 * g.K * 2, lw.w_up + (int64_t)lr * g.K, bytes);
                 ++issued;
                 row += n;
                 continue;
@@ -382,39 +394,92 @@ struct Producer {
                     for (int32_t j0 = 0; j0 < n; j0 += g.rps) {
                         const int32_t cnt = min(g.rps, n - j0);
                         uint32_t s;
-                        if (!acquire_slot(c, &s)) return false;
                         const uint32_t bytes = (uint32_t)(cnt * g.K * 2);
-                        mbar_arrive_expect_tx(&c.sc->full[s], bytes);
-                        bulk_g2s(c.ring + (size_t)s * slot_bytes, Wm + (int64_t)(lr + j0) * g.K, bytes, &c.sc->full[s],
-                                 pol);
+                        if (!begin_slot(c, &s, bytes)) return false;
+                        copy(c, s, c.ring + (size_t)s * slot_bytes, Wm + (int64_t)(lr + j0) * g.K, bytes);
                         ++issued;
                     }
                 }
                 row += n;
                 continue;
             }
+            if (g.ksplit > kMvResident) return run_matvec_long(c, t, g, lw, row);
             for (int32_t ks = 0; ks < g.ksplit; ++ks) {
-                uint32_t s;
-                if (!acquire_slot(c, &s)) return false;
                 const int32_t k0 = ks * g.kc;
                 const int32_t pw = min(g.kc, g.K - k0);
                 const uint32_t bytes = (uint32_t)(g.row_mult * n * pw * 2);
+                uint32_t s;
+                if (!begin_slot(c, &s, bytes)) return false;
                 uint8_t *dst = c.ring + (size_t)s * slot_bytes;
-                mbar_arrive_expect_tx(&c.sc->full[s], bytes);
                 for (int m = 0; m < g.row_mult; ++m) {
                     const uint16_t *Wm = (m == 0) ? W : lw.w_up;
                     if (g.ksplit == 1) {
-                        bulk_g2s(dst + (size_t)m * n * pw * 2, Wm + (int64_t)lr * g.K, (uint32_t)(n * pw * 2),
-                                 &c.sc->full[s], pol);
+                        copy(c, s, dst + (size_t)m * n * pw * 2, Wm + (int64_t)lr * g.K, (uint32_t)(n * pw * 2));
                     } else {
                         for (int32_t r = 0; r < n; ++r)
-                            bulk_g2s(dst + (size_t)(m * n + r) * pw * 2, Wm + (int64_t)(lr + r) * g.K + k0,
-                                     (uint32_t)(pw * 2), &c.sc->full[s], pol);
+                            copy(c, s, dst + (size_t)(m * n + r) * pw * 2, Wm + (int64_t)(lr + r) * g.K + k0,
+                                 (uint32_t)(pw * 2));
                     }
                 }
                 ++issued;
             }
             row += n;
+        }
+        return true;
+    }
+
+    // Rows of inputs longer than kMvResident pieces, from `row` on: up to
+    // kMvSuper row groups at a time, piece by piece (piece ks of every group
+    // of the super-group, then piece ks + 1), the order in which the compute
+    // warps consume them, so that each input piece they load from L2 serves
+    // every group of the super-group.  A slot holds piece ks of one group's
+    // rows (gate rows, then up rows), one bulk copy per row.
+    __device__ bool run_matvec_long(const Ctx &c, const Task &t, const MvGeom &g, const LayerW &lw, int32_t row) {
+        const KParams &p = *c.p;
+        const int op = t.op;
+        const int32_t qb1 = p.nq * p.d, qb2 = qb1 + p.nkv * p.d, qb3 = p.qkv_rows;
+        while (row < t.a1) {
+            int32_t gr[kMvSuper], gn[kMvSuper];
+            int ng = 0;
+            for (int32_t r = row; ng < kMvSuper && r < t.a1; ++ng) {
+                int32_t n = min(g.rpp, t.a1 - r);
+                if (op == OP_QKV) n = min(n, (r < qb1 ? qb1 : (r < qb2 ? qb2 : qb3)) - r);
+                gr[ng] = r;
+                gn[ng] = n;
+                r += n;
+            }
+            for (int32_t ks = 0; ks < g.ksplit; ++ks) {
+                const int32_t k0 = ks * g.kc;
+                const int32_t pw = min(g.kc, g.K - k0);
+                if (op == OP_DOWN && p.down_maps != nullptr) {
+                    // one 3-D TMA copy per slot: piece ks of rpp rows (rows
+                    // past the group's own belong to the next group or read as 0)
+                    const void *map = p.down_maps + (size_t)t.layer * 128;
+                    for (int gi = 0; gi < ng; ++gi) {
+                        uint32_t s;
+                        if (!begin_slot(c, &s, (uint32_t)(g.rpp * g.kc * 2))) return false;
+                        tma_load_3d(c.ring + (size_t)s * slot_bytes, map, 0, k0 / 256, gr[gi], &c.sc->full[s], pol);
+                        ++issued;
+                    }
+                    continue;
+                }
+                for (int gi = 0; gi < ng; ++gi) {
+                    const int32_t n = gn[gi];
+                    uint32_t s;
+                    if (!begin_slot(c, &s, (uint32_t)(g.row_mult * n * pw * 2))) return false;
+                    int32_t lr;
+                    const uint16_t *W = mv_matrix(p, op, lw, gr[gi], &lr);
+                    uint8_t *dst = c.ring + (size_t)s * slot_bytes;
+                    for (int m = 0; m < g.row_mult; ++m) {
+                        const uint16_t *Wm = (m == 0) ? W : lw.w_up;
+                        for (int32_t r = 0; r < n; ++r)
+                            copy(c, s, dst + (size_t)(m * n + r) * pw * 2, Wm + (int64_t)(lr + r) * g.K + k0,
+                                 (uint32_t)(pw * 2));
+                    }
+                    ++issued;
+                }
+            }
+            row = gr[ng - 1] + gn[ng - 1];
         }
         return true;
     }
@@ -463,9 +528,8 @@ struct Producer {
                 (int32_t)((((int64_t)t.layer * p.num_pages + pg) * p.nkv + t.a1) * p.page_size + tok0 % p.page_size);
             for (int j = 0; j < kAttnBlock / ts; ++j) {
                 uint32_t s;
-                if (!acquire_slot(c, &s)) return false;
+                if (!begin_slot(c, &s, (uint32_t)(2 * halves * ts * 128))) return false;
                 uint8_t *dst = c.ring + (size_t)s * slot_bytes;
-                mbar_arrive_expect_tx(&c.sc->full[s], (uint32_t)(2 * halves * ts * 128));
                 for (int h = 0; h < halves; ++h) {
                     tma_load_2d(dst + (size_t)h * ts * 128, p.kv_maps[0], h * 64, row0 + j * ts, &c.sc->full[s], pol);
                     tma_load_2d(dst + (size_t)(halves + h) * ts * 128, p.kv_maps[1], h * 64, row0 + j * ts,
@@ -958,14 +1022,6 @@ struct Consumer {
                 }
             }
         }
-        // streamed inputs: the pieces of the next kMvAhead slots, loaded ahead
-        // (a ring of register buffers; slot ks uses buffer ks % kMvAhead)
-        float xq[kMvAhead][8];
-        if (!resident) {
-#pragma unroll
-            for (int a = 0; a < kMvAhead; ++a) load_piece(p, xin, emb_row, gain, rn, nchunk, a % g.ksplit, xq[a]);
-        }
-
         const int lq = lane >> 2;  // row this lane holds after the reduce-scatter
         // group geometry and outputs in registers (the ring's inline asm would
         // otherwise force re-reads of the parameter block every slot)
@@ -974,75 +1030,108 @@ struct Consumer {
         const uint16_t *const embed_row = p.embed + (int64_t)token * p.H;
         int32_t pg = 0;  // row groups waiting in mv_part
         unsigned long long best = 0ull;  // fused greedy pick: this thread's best packed logit
-        for (int32_t row = t.a0; row < t.a1;) {
-            int32_t n = min(g.rpp, t.a1 - row);
-            if (op == OP_QKV) n = min(n, (row < qb1 ? qb1 : (row < qb2 ? qb2 : qb3)) - row);
-            const int32_t R = n * g.row_mult;
-            uint64_t acc2[8];
-#pragma unroll
-            for (int r = 0; r < 8; ++r) acc2[r] = 0ull;
-            if (g.rps == 8) {
-                // 8 rows of one matrix, or 4 gate rows (acc 0..3) + 4 up rows (acc 4..7)
-                if (g.row_mult == 2) mv_rows8_gu(c, n, nchunk, xr[0], acc2);
-                else mv_rows8(c, n, nchunk, xr[0], acc2);
-            } else if (g.rps == 4) {
-                // acc rows 0..3: first slot; 4..7: the up rows (gate/up) or rows 4..7
-                const int32_t na = (g.row_mult == 2) ? n : min(n, 4), nb = (g.row_mult == 2) ? n : n - 4;
-                if (g.ksplit == 2) {
-                    mv_rows4<2>(c, na, nchunk, xr, &acc2[0]);
-                    if (nb > 0) mv_rows4<2>(c, nb, nchunk, xr, &acc2[4]);
-                } else {
-                    mv_rows4<1>(c, na, nchunk, xr, &acc2[0]);
-                    if (nb > 0) mv_rows4<1>(c, nb, nchunk, xr, &acc2[4]);
-                }
-            } else if (g.ksplit == 2) {
-                mv_group2(c, g.kc >> 3, (g.K - g.kc) >> 3, R, xr[0], xr[1], acc2);
-            } else if (resident) {
-#pragma unroll
-                for (int ks = 0; ks < kMvResident; ++ks)
-                    if (ks < g.ksplit) mv_slot(c, min(g.kc, g.K - ks * g.kc) >> 3, R, xr[ks], acc2);
-            } else {
-                for (int ks = 0; ks < g.ksplit; ++ks) {
-                    // oldest buffer out, the piece needed kMvAhead slots from now in
-                    // (wrapping into the next group)
-                    float xc[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        xc[e] = xq[0][e];
-#pragma unroll
-                        for (int a = 0; a + 1 < kMvAhead; ++a) xq[a][e] = xq[a + 1][e];
-                    }
-                    load_piece(p, xin, emb_row, gain, rn, nchunk, (ks + kMvAhead) % g.ksplit, xq[kMvAhead - 1]);
-                    mv_slot(c, min(g.kc, g.K - ks * g.kc) >> 3, R, xc, acc2);
-                }
-            }
-            // reduce-scatter of the 8 row sums over the warp: lane l ends with
-            // value l/4; this warp's totals wait in shared memory, so the warps
-            // never meet per group (they drift apart by up to the ring's depth)
+        // a group's 8 row sums, reduced over the warp: lane l ends with value
+        // l/4; this warp's totals wait in shared memory, so the warps never
+        // meet per group (they drift apart by up to the ring's depth)
+        auto park = [&](const uint64_t (&acc2)[8], int32_t grow, int32_t gn) {
             float acc[8];
 #pragma unroll
             for (int r = 0; r < 8; ++r) acc[r] = sum_x2(acc2[r]);
             const float v = warp_reduce8(acc, lane);
             if ((lane & 3) == 0) c.sc->mv_part[pg][lq][wc] = v;
             if (ct == 0) {
-                c.sc->mv_grow[pg] = row;
-                c.sc->mv_gn[pg] = n;
+                c.sc->mv_grow[pg] = grow;
+                c.sc->mv_gn[pg] = gn;
             }
             ++pg;
-            row += n;
-            if (pg == kPartGroups || row >= t.a1) {
-                if (!resid_stored) {
+        };
+        // every warp's totals of the waiting groups are in: finish them
+        auto flush = [&](bool more) {
+            if (!resid_stored) {
 #pragma unroll
-                    for (int k = 0; k < kMaxResid / kComputeThreads; ++k) {
-                        const int32_t i = ct + k * kComputeThreads;
-                        if (i < nrows) c.sc->resid[i] = rv[k];
-                    }
-                    resid_stored = true;
+                for (int k = 0; k < kMaxResid / kComputeThreads; ++k) {
+                    const int32_t i = ct + k * kComputeThreads;
+                    if (i < nrows) c.sc->resid[i] = rv[k];
                 }
-                compute_bar();  // every warp's totals of the waiting groups are in
-                mv_finish(c, t, g, pg, resid_in_smem, out_qkv, out_x, out_h, out_logits, embed_row, best);
-                pg = 0;
-                if (row < t.a1) compute_bar();  // the buffer is refilled
+                resid_stored = true;
+            }
+            compute_bar();
+            mv_finish(c, t, g, pg, resid_in_smem, out_qkv, out_x, out_h, out_logits, embed_row, best);
+            pg = 0;
+            if (more) compute_bar();  // the buffer is refilled
+        };
+        if (!resident) {
+            // Inputs longer than kMvResident pieces stream from L2.  Up to
+            // kMvSuper row groups go through the pieces together (the
+            // producer's order), so each piece is loaded once for all of them,
+            // one piece (that is, up to kMvSuper slots) ahead of its use.
+            float xc[8], xn[8];
+            load_piece(p, xin, emb_row, gain, rn, nchunk, 0, xc);
+            for (int32_t row = t.a0; row < t.a1;) {
+                int32_t gr[kMvSuper], gn[kMvSuper];
+                int32_t r = row;
+#pragma unroll
+                for (int gi = 0; gi < kMvSuper; ++gi) {
+                    int32_t n = 0;
+                    if (r < t.a1) {
+                        n = min(g.rpp, t.a1 - r);
+                        if (op == OP_QKV) n = min(n, (r < qb1 ? qb1 : (r < qb2 ? qb2 : qb3)) - r);
+                    }
+                    gr[gi] = r;
+                    gn[gi] = n;
+                    r += n;
+                }
+                uint64_t acc2[kMvSuper][8];
+#pragma unroll
+                for (int gi = 0; gi < kMvSuper; ++gi)
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) acc2[gi][q] = 0ull;
+                for (int ks = 0; ks < g.ksplit; ++ks) {
+                    // the next piece (piece 0 after the last: the next super-group's first)
+                    load_piece(p, xin, emb_row, gain, rn, nchunk, ks + 1 < g.ksplit ? ks + 1 : 0, xn);
+                    const int32_t pw8 = min(g.kc, g.K - ks * g.kc) >> 3;
+#pragma unroll
+                    for (int gi = 0; gi < kMvSuper; ++gi)
+                        if (gn[gi] > 0) mv_slot(c, pw8, gn[gi] * g.row_mult, xc, acc2[gi]);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) xc[e] = xn[e];
+                }
+#pragma unroll
+                for (int gi = 0; gi < kMvSuper; ++gi)
+                    if (gn[gi] > 0) park(acc2[gi], gr[gi], gn[gi]);
+                row = r;
+                if (pg + kMvSuper > kPartGroups || row >= t.a1) flush(row < t.a1);
+            }
+        } else {
+            for (int32_t row = t.a0; row < t.a1;) {
+                int32_t n = min(g.rpp, t.a1 - row);
+                if (op == OP_QKV) n = min(n, (row < qb1 ? qb1 : (row < qb2 ? qb2 : qb3)) - row);
+                const int32_t R = n * g.row_mult;
+                uint64_t acc2[8];
+#pragma unroll
+                for (int r = 0; r < 8; ++r) acc2[r] = 0ull;
+                if (g.rps == 8) {
+                    // 8 rows of one matrix, or 4 gate rows (acc 0..3) + 4 up rows (acc 4..7)
+                    if (g.row_mult == 2) mv_rows8_gu(c, n, nchunk, xr[0], acc2);
+                    else mv_rows8(c, n, nchunk, xr[0], acc2);
+                } else if (g.rps == 4) {
+                    // acc rows 0..3: first slot; 4..7: the up rows (gate/up) or rows 4..7
+                    const int32_t na = (g.row_mult == 2) ? n : min(n, 4), nb = (g.row_mult == 2) ? n : n - 4;
+                    if (g.ksplit == 2) {
+                        mv_rows4<2>(c, na, nchunk, xr, &acc2[0]);
+                        if (nb > 0) mv_rows4<2>(c, nb, nchunk, xr, &acc2[4]);
+                    } else {
+                        mv_rows4<1>(c, na, nchunk, xr, &acc2[0]);
+                        if (nb > 0) mv_rows4<1>(c, nb, nchunk, xr, &acc2[4]);
+                    }
+                } else if (g.ksplit == 2) {
+                    mv_group2(c, g.kc >> 3, (g.K - g.kc) >> 3, R, xr[0], xr[1], acc2);
+                } else {
+                    mv_slot(c, g.K >> 3, R, xr[0], acc2);
+                }
+                park(acc2, row, n);
+                row += n;
+                if (pg == kPartGroups || row >= t.a1) flush(row < t.a1);
             }
         }
         if (op == OP_LM && p.greedy) {
@@ -1660,6 +1749,35 @@ struct Consumer {
                     }
             }
             compute_bar();
+        }
+        if (r.n_live == 1) {
+            // The only split with work (at most one cached block, or one
+            // split in all): normalise in registers and write the heads'
+            // outputs; no partial, no split counter, no merge.  The result is
+            // the merge's for one split, bit for bit (its weight is exp(0)).
+            if (wc < nks) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float v = oacc[0][i];
+                    if (G == 8) v += oacc[1][i];
+                    else if (G == 1) v = (i & 1) ? 0.f : oacc[0][i] + oacc[0][i + 1];
+                    else v += __shfl_xor_sync(0xFFFFFFFFu, v, partner);
+                    const int e = 16 * wc + tr + (i >> 1) * 8;
+                    const int head = (G == 1) ? 0 : 2 * cq + (i & 1);
+                    const bool live = head_lane && (G != 1 || (i & 1) == 0);
+                    if (live) {
+                        const float o = v * (1.f / sc->att_l[head]);
+                        const int64_t col = (int64_t)(kvh * G + head) * d + e;
+                        if (p.tc) store_split(p.attn_a, p.nq * d, p.npad, b, col, o);
+                        else p.attn_out[(int64_t)b * p.nq * d + col] = o;
+                    }
+                }
+            }
+            if (p.tc) fence_proxy_async_global();  // read next by the O projection's TMA
+            compute_bar();
+            if (ct == 0 && p.only_op < 0 && t.signal_ev != kNoEvent && !local_abort(c))
+                red_release_gpu_add(p.ctl + t.signal_ev, 1u);  // cumulative: every output written before the barrier
+            return;
         }
         // partial result of this split: unnormalised o (high + low columns), running max, sum
         const int64_t pidx = (((int64_t)b * p.nkv + kvh) * S + t.a2) * G;

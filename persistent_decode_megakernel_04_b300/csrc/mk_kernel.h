@@ -23,7 +23,8 @@ constexpr int kAttnStep = 2 * kAttnBlock;    // cached tokens an attention step 
 constexpr int kPhlStride = kAttnStep + 8;    // bf16 row stride of the split softmax weights
 constexpr int kMaxResid = 512;    // residual rows prefetched per matvec task
 constexpr int kMvResident = 2;    // matvec inputs of up to 2 x 2048 columns stay in registers
-constexpr int kMvAhead = 3;       // longer inputs: pieces loaded this many slots ahead
+constexpr int kMvSuper = 2;       // longer inputs: row groups that stream piece by piece together, so that
+                                  // each input piece is loaded once for all of them
 constexpr int kMaxASlots = 8;     // activation ring slots (batched path)
 
 struct KParams {
@@ -56,6 +57,11 @@ struct KParams {
     int32_t slot_bytes, num_slots, attn_ts, attn_splits;  // attn_ts: KV tokens per ring slot
     int32_t l2_prefetch_bytes;
     int32_t max_inflight;  // ring copies in flight per CTA (0 or >= num_slots: no limit)
+    // batch 1: per-layer tensor maps of w_down seen as [H][I/256][256] bf16,
+    // boxes of rpp rows x kc/256 blocks x 256 columns, so that one TMA copy
+    // fills a ring slot with piece ks of a row group (nullptr: one bulk copy
+    // per row and piece)
+    const uint8_t *down_maps;
     // launch mode
     int32_t only_op;     // -1: every task (persistent mode); else one operator of one layer
     int32_t only_layer;
@@ -107,6 +113,12 @@ cudaError_t megakernel_set_smem(int variant, size_t smem);
 
 // Host: TMA maps of the K and V pools (KParams::kv_maps) for tiles of ts tokens.
 bool encode_kv_maps(KParams &k, const mk_model_cfg &c, const mk_kv_cache &kv, int32_t ts);
+
+// Host: whether batch-1 down-projection slots can come from one 3-D TMA copy
+// each (pieces of 2048 columns, rows a multiple of them), and the map of one
+// layer's w_down (128 bytes at m).
+bool down_tma_ok(const MvGeom &g);
+bool encode_down_map(void *m, const void *w_down, const MvGeom &g);
 
 cudaError_t launch_rope_table(float2 *rope, int32_t max_seq, int32_t d, float theta, cudaStream_t stream);
 cudaError_t launch_greedy_next(const float *logits, int32_t B, int32_t V, int32_t *tokens, int32_t *positions,

@@ -180,6 +180,17 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int32_t
         : "memory");
 }
 
+// 3-D tiled TMA load of box {x.., y.., z..} of the tensor map into shared
+// memory; completion counted on `bar` in bytes.
+__device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int32_t x, int32_t y, int32_t z,
+                                            uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
 // generic-proxy writes <-> async-proxy (TMA, MMA) reads
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }

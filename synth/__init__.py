@@ -17,8 +17,11 @@ import numpy as np
 
 from .configs import (  # noqa: F401  (re-exported)
     TINY_D128,
+    TINY_FFN6K,
     TINY_G8,
+    TINY_LONGFF,
     TINY_MHA,
+    TINY_WIDE,
     LAYER_TIDS,
     TID_EMBED,
     TID_FINAL_NORM,

@@ -56,6 +56,18 @@ TINY = ModelCfg("tiny", 2, 256, 4, 2, 64, 688, 1024, rope_theta=1e4)
 TINY_G8 = ModelCfg("tiny-g8", 2, 256, 16, 2, 64, 688, 1024, rope_theta=1e4)
 TINY_MHA = ModelCfg("tiny-mha", 2, 256, 4, 4, 64, 688, 1024, rope_theta=1e4)
 TINY_D128 = ModelCfg("tiny-d128", 2, 512, 8, 2, 128, 1376, 1024, rope_theta=1e4)
+# tiny variants whose batch-1 matvec inputs are longer than the 4096 columns
+# kept in registers: a wide hidden size (QKV, gate/up and LM-head inputs of
+# 4608 columns, the last 2048-column piece ragged) and a wide feed-forward
+# (down-projection input of 5000 columns)
+# (weights N(0, 0.01): with 0.02 the wide q and k make the softmax sharp
+# enough that rounding the cache to bf16 alone moves the logits by up to
+# 2.9e-2 against the fp64 oracle, at the edge of the tolerance)
+TINY_WIDE = ModelCfg("tiny-wide", 2, 4608, 4, 2, 128, 688, 1024, rope_theta=1e4, weight_std=0.01)
+TINY_LONGFF = ModelCfg("tiny-longff", 2, 256, 4, 2, 64, 5000, 1024, rope_theta=1e4)
+# a feed-forward width that is a multiple of 2048: the batch-1 down projection
+# then fills each ring slot with one 3-D TMA copy instead of one copy per row
+TINY_FFN6K = ModelCfg("tiny-ffn6144", 2, 256, 4, 2, 64, 6144, 1024, rope_theta=1e4)
 LLAMA_1B = ModelCfg("llama-3.2-1b-shaped", 16, 2048, 32, 8, 64, 8192, 128256, rope_theta=5e5, tied_embeddings=True)
 LLAMA_8B = ModelCfg("llama-3-8b-shaped", 32, 4096, 32, 8, 128, 14336, 128256, rope_theta=5e5)
 LLAMA_70B = ModelCfg("llama-70b-shaped", 80, 8192, 64, 8, 128, 28672, 128256, rope_theta=5e5)

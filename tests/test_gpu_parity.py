@@ -271,3 +271,21 @@ def test_fused_greedy_step_matches_step_then_pick(cuda_device, name, batch):
         assert torch.equal(logits_a, logits_b), f"step {step}: logits differ"
         assert torch.equal(tok_a, tok_b) and torch.equal(pos_a, pos_b), f"step {step}: {tok_a} {tok_b} {pos_a} {pos_b}"
         assert int(pos_b[0]) == 41 + step
+
+
+@pytest.mark.parametrize("m", [synth.TINY_WIDE, synth.TINY_LONGFF, synth.TINY_FFN6K],
+                         ids=["wide-hidden", "wide-ffn", "ffn-6144-tma"])
+@pytest.mark.parametrize("opts", [None, dict(num_ctas=7, attn_splits=3), dict(num_ctas=2, attn_splits=1)],
+                         ids=["all-sms", "7ctas", "2ctas"])
+def test_tiny_long_matvec_inputs(cuda_device, m, opts):
+    """Batch-1 projections whose input is longer than the 4096 columns kept
+    in registers stream the input from L2 piece by piece, with row groups
+    taken several at a time: QKV, gate/up and the LM head of a 4608-wide
+    hidden size (a ragged last piece, groups cut at the q/k/v boundaries) and
+    the down projection of a 5000-wide feed-forward (one bulk copy per row
+    and piece) and of a 6144-wide one (one 3-D TMA copy per slot, row groups
+    cut short at the CTA's range end).  Two CTAs hold 512 or more rows each,
+    so the per-group totals are flushed mid-task."""
+    plan, kv = harness.gpu_plan(m, 128, opts=mk.mk_plan_options(**opts) if opts else None)
+    model = harness.oracle_model(m)
+    harness.run_teacher_forced(plan, kv, model, synth.tokens(24, 0, 13, m.vocab), 4, 128)
