@@ -154,52 +154,112 @@ class ClockSampler:
 
 # ----------------------------------------------------------------- CPU side
 
-def oracle_sample(m, steps: int, pos0: int, seed: int = 0, n_layers_gen: int = 2):
-    """Times the fp64 oracle, as it stands, on a bounded sample of the decode
-    step: each sample is ONE decoder layer (cycling over n_layers_gen
-    generated layers) plus 1/n_layers of the LM-head rows, so n_layers
-    samples cost one whole token.  Returns (ms per token, threads, text)."""
+def _host_budget_bytes() -> int:
+    """Host memory the oracle's weights may take: half the machine's RAM."""
+    try:
+        return os.sysconf("SC_PAGE_SIZE") * os.sysconf("SC_PHYS_PAGES") // 2
+    except (ValueError, OSError):
+        return 32 << 30
+
+
+def oracle_steps(m, pos0: int, steps: int, warm: int = 1, threads: int = 0, seed: int = 0, model=None):
+    """Times WHOLE decode steps of the fp64 oracle, as it stands: every layer
+    and the full LM head, at positions pos0, pos0+1, ... (context pos0+1, ...,
+    the positions the GPU arm times).  The cache's first pos0 positions hold
+    the seeded stand-in contents: a step's cost does not depend on what the
+    cache holds, only on its length.  `warm` untimed steps come first; each
+    step feeds the previous one's greedy token.  threads > 0 sets the
+    oracle's team size.  A model whose weights do not fit half the host's
+    memory (the 70B shape) is timed layer by layer, each layer's weights
+    generated untimed before its part of the step.
+    Returns (list of ms per step, threads used, model)."""
     import oracle
 
-    layers = [synth.host_layer_weights(m, seed, l) for l in range(n_layers_gen)]
-    rows = max(1, m.vocab // m.n_layers)
-    head = synth.normal_bf16((rows, m.hidden), seed, synth.TID_LM_HEAD, m.weight_std)
-    fin = synth.normal_bf16((m.hidden,), seed, synth.TID_FINAL_NORM, 0.0, 1.0)
-    emb = synth.normal_bf16((1, m.hidden), seed, synth.TID_EMBED, m.weight_std)
-    model = oracle.Model(replace(m, vocab=rows), {"embed": emb, "lm_head": head, "final_norm": fin})
-    max_seq = pos0 + steps + 1
-    kc = np.zeros((max_seq, m.n_kv_heads, m.head_dim))
-    vc = np.zeros_like(kc)
-    x = model.embed_token(0)
+    if threads > 0:
+        oracle.set_num_threads(threads)
+    streamed = model is None and synth.weight_bytes(m) > _host_budget_bytes()
+    if model is None:
+        if streamed:
+            emb = synth.normal_bf16((m.vocab, m.hidden), seed, synth.TID_EMBED, m.weight_std)
+            lm = synth.normal_bf16((m.vocab, m.hidden), seed, synth.TID_LM_HEAD, m.weight_std)
+            fin = synth.normal_bf16((m.hidden,), seed, synth.TID_FINAL_NORM, 0.0, 1.0)
+            model = oracle.Model(m, {"embed": emb, "lm_head": lm, "final_norm": fin})
+        else:
+            model = oracle.Model(m, synth.host_weights(m, seed))
+    max_seq = pos0 + warm + steps + 1
+    if streamed:
+        kc = np.zeros((max_seq, m.n_kv_heads, m.head_dim))
+        vc = np.zeros_like(kc)
+    else:
+        kc, vc = model.new_cache(max_seq)
+        for l in range(m.n_layers):
+            kc[l, :pos0] = synth.bf16_to_f64(synth.host_kv(m, seed, l, "k", 1, pos0)[0])
+            vc[l, :pos0] = synth.bf16_to_f64(synth.host_kv(m, seed, l, "v", 1, pos0)[0])
+    tok = int(synth.tokens(1, seed, 0, m.vocab)[0])
     times = []
-    for i in range(steps):
-        t0 = time.perf_counter()
-        model.layer_step(layers[i % n_layers_gen], kc, vc, pos0 + i, x)
-        model.head(x)
-        times.append(time.perf_counter() - t0)
-    per_token_ms = 1e3 * statistics.mean(times) * m.n_layers
-    threads = oracle.num_threads()
-    desc = (f"{steps} samples of one {m.name} decoder layer + 1/{m.n_layers} of the LM-head rows at positions "
-            f"{pos0}..{pos0 + steps - 1}, fp64 oracle, scaled x{m.n_layers} to one token")
-    return per_token_ms, threads, desc
+    for i in range(warm + steps):
+        if streamed:
+            x = model.embed_token(tok)
+            dt = 0.0
+            for l in range(m.n_layers):
+                lw = synth.host_layer_weights(m, seed, l)
+                kc[:pos0] = synth.bf16_to_f64(synth.host_kv(m, seed, l, "k", 1, pos0)[0])
+                vc[:pos0] = synth.bf16_to_f64(synth.host_kv(m, seed, l, "v", 1, pos0)[0])
+                t0 = time.perf_counter()
+                model.layer_step(lw, kc, vc, pos0 + i, x)
+                dt += time.perf_counter() - t0
+            t0 = time.perf_counter()
+            logits = model.head(x)
+            dt += time.perf_counter() - t0
+        else:
+            t0 = time.perf_counter()
+            logits = model.decode_step(kc, vc, tok, pos0 + i)
+            dt = time.perf_counter() - t0
+        if i >= warm:
+            times.append(dt * 1e3)
+        tok = int(np.argmax(logits))
+    return times, oracle.num_threads(), model
+
+
+def cpu_baseline(m, pos0: int, steps: int, single_thread_steps: int):
+    """The oracle on all the host cores it runs with by default (`steps`
+    whole decode steps) and on one thread (`single_thread_steps` steps), at
+    the positions the GPU arm times."""
+    import oracle
+
+    default_threads = oracle.num_threads()
+    ms, threads, model = oracle_steps(m, pos0, steps)
+    out = {"value": statistics.mean(ms), "unit": "ms/token", "cores": threads, "kind": "oracle",
+           "sample": f"{steps} whole decode steps of the {m.name} fp64 oracle (every layer, full LM head) at "
+                     f"positions {pos0}..{pos0 + steps - 1}, after 1 untimed step"}
+    if single_thread_steps > 0:
+        ms1, t1, _ = oracle_steps(m, pos0, single_thread_steps, warm=0, threads=1, model=model)
+        out["single_thread"] = {"value": statistics.mean(ms1), "unit": "ms/token", "cores": t1,
+                                "sample": f"{single_thread_steps} whole decode step(s) from position {pos0}"}
+        oracle.set_num_threads(default_threads)
+    return out
 
 
 def run_reference(args, wl):
     if int(os.environ.get("RANK", "0")) != 0:
         return
     m = wl.model
-    oracle_sample(m, args.warmup, wl.prompt_len)
-    ms, threads, desc = oracle_sample(m, args.steps, wl.prompt_len)
+    # the same context lengths as the GPU arm's timed steps: prompt, then the warm-up steps
+    pos0 = wl.prompt_len + args.warmup
+    ms, threads, _ = oracle_steps(m, pos0, args.steps, warm=args.warmup)
+    value = statistics.mean(ms)
+    desc = (f"{args.steps} whole decode steps of the {m.name} fp64 oracle (every layer, full LM head) at "
+            f"positions {pos0}..{pos0 + args.steps - 1}, after {args.warmup} untimed steps")
     line = {
-        "impl": "reference", "metric": METRIC, "value": ms, "unit": "ms/token", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False,
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "ms/token", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": value, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded random-init weights)",
         "config": {"workload": args.workload, "model": m.name, "batch": wl.batch, "prompt_len": wl.prompt_len,
                    "context": "seeded paged cache" if seeded_context(wl) else "prefilled prompt",
-                   "ctx_first_timed": wl.prompt_len + 1, "ctx_last_timed": wl.prompt_len + args.steps,
+                   "ctx_first_timed": pos0 + 1, "ctx_last_timed": pos0 + args.steps,
                    "parallelism": "replicas x1"},
-        "cpu_baseline": {"value": ms, "unit": "ms/token", "cores": threads, "kind": "oracle", "sample": desc},
-        "e2e": {"value": ms, "unit": "ms/token", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "cpu_baseline": {"value": value, "unit": "ms/token", "cores": threads, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "ms/token", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
@@ -443,8 +503,7 @@ def run_mk(args, wl):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        ms, threads, desc = oracle_sample(m, args.cpu_samples, wl.prompt_len)
-        cpu = {"value": ms, "unit": "ms/token", "cores": threads, "kind": "oracle", "sample": desc}
+        cpu = cpu_baseline(m, ctx0 - 1, args.cpu_samples, args.cpu_single_thread_steps)
 
     if rank == 0:
         line = {
@@ -488,7 +547,9 @@ def main():
     ap.add_argument("--workload", default="8b", choices=sorted(WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=32)
     ap.add_argument("--ablation-steps", type=int, default=8)
-    ap.add_argument("--cpu-samples", type=int, default=16)
+    ap.add_argument("--cpu-samples", type=int, default=8, help="whole oracle decode steps timed on all host cores")
+    ap.add_argument("--cpu-single-thread-steps", type=int, default=1,
+                    help="whole oracle decode steps timed on one host thread (0: skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prompt-len", type=int, default=0, help="override the workload's prompt length")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (sequences per step)")

@@ -68,6 +68,8 @@ def lib():
         L = ctypes.CDLL(str(LIB_PATH))
         L.orc_num_threads.restype = _i
         L.orc_num_threads.argtypes = []
+        L.orc_set_num_threads.restype = None
+        L.orc_set_num_threads.argtypes = [_i]
         L.orc_bf16.restype = _d
         L.orc_bf16.argtypes = [ctypes.c_uint16]
         L.orc_rmsnorm.argtypes = [_i, _p, _p, _d, _p]
@@ -88,6 +90,11 @@ def lib():
 def num_threads() -> int:
     """Threads the oracle's parallel loops run with in this process."""
     return int(lib().orc_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads for the oracle's later parallel loops (timing runs only)."""
+    lib().orc_set_num_threads(int(n))
 
 
 def _f64(a) -> np.ndarray:

@@ -70,6 +70,12 @@ int orc_num_threads(void) {
     return n;
 }
 
+/* Team size of the later parallel loops of this library (timing only; no
+ * arithmetic: every output row is still one sequential sum). */
+void orc_set_num_threads(int n) {
+    if (n > 0) omp_set_num_threads(n);
+}
+
 double orc_bf16(uint16_t h) {
     uint32_t u = (uint32_t)h << 16;
     float f;

@@ -131,3 +131,20 @@ def test_cpu_baseline_reports_the_threads_the_oracle_ran_with():
     assert r.returncode == 0, r.stderr
     d = json.loads([l for l in r.stdout.splitlines() if l.strip()][-1])
     assert d["cpu_baseline"]["cores"] == 2
+
+
+def test_cpu_baseline_times_whole_oracle_steps_on_all_cores_and_one_thread():
+    """Whole decode steps (every layer and the full LM head), not extrapolated
+    samples: the step count asked for, on the default team and on one thread."""
+    sys.path.insert(0, str(ROOT))
+    import bench
+    import oracle
+    from synth import WORKLOADS
+
+    m = WORKLOADS["tiny"].model
+    ms, threads, model = bench.oracle_steps(m, 40, 3)
+    assert len(ms) == 3 and all(t > 0 for t in ms) and threads == oracle.num_threads()
+    cb = bench.cpu_baseline(m, 40, 2, 1)
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and "whole decode steps" in cb["sample"]
+    assert cb["single_thread"]["cores"] == 1 and cb["single_thread"]["value"] > 0
+    assert oracle.num_threads() == cb["cores"]  # the default team is restored

@@ -79,7 +79,7 @@ def test_batched_rows_equal_single_sequence_runs(cuda_device):
         harness.compare_logits(got[b], l1.cpu().numpy()[0], f"row {b} vs batch-1 run")
 
 
-@pytest.mark.parametrize("B", [8, 64])
+@pytest.mark.parametrize("B", [8, 32, 64])
 def test_8b_batched_decode_from_seeded_cache(cuda_device, B):
     """The 8B-shaped decoder at 4096 cached tokens per sequence (paged,
     shuffled pages), in the launch configuration the bench times; the oracle

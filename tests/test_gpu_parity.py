@@ -217,6 +217,27 @@ def test_full_size_decode_from_seeded_cache(cuda_device, name, ctx, steps):
     print(name, stats)
 
 
+@pytest.mark.parametrize("name,steps", [("8b", 16), ("1b", 8)])
+def test_full_size_prompt_prefill_and_greedy_decode(cuda_device, name, steps):
+    """The stated workloads end to end at full size, in the launch
+    configuration the bench times (every SM, default ring): the 8B-shaped
+    decoder's 39-token random prompt and the 1B-shaped decoder's 512-token
+    random-ID context, prefilled through mk_prefill on the GPU and token by
+    token by the oracle, then teacher-forced greedy decode steps, the logits
+    compared at every step.  The cache holds the keys and values the model
+    itself computed for the prompt (rounded to bf16 on the GPU, fp64 in the
+    oracle)."""
+    wl = WORKLOADS[name]
+    m = wl.model
+    max_seq = ((wl.prompt_len + steps + 8 + 63) // 64) * 64
+    plan, kv = harness.gpu_plan(m, max_seq)
+    model = harness.oracle_model(m)
+    prompt = synth.tokens(wl.prompt_len, wl.seed, 0, m.vocab)
+    stats = harness.run_teacher_forced(plan, kv, model, prompt, steps, max_seq)
+    assert len(stats) == steps + 1
+    print(name, "rel-L2", [round(x["rel_l2"], 5) for x in stats], "max-abs", [round(x["max_abs"], 4) for x in stats])
+
+
 @pytest.mark.parametrize("m", [synth.TINY_G8, synth.TINY_MHA, synth.TINY_D128], ids=["g8", "mha", "d128"])
 def test_tiny_variants_group_sizes_and_head_dim(cuda_device, m):
     """GQA groups of 8 and 1 (two and one MMA column tiles in attention) and
