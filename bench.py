@@ -366,11 +366,11 @@ def run_mk(args, wl):
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     # The timed steps replay CUDA graphs of the step: a serving loop launches
     # it that way, and for the small shapes the host's per-launch work would
-    # otherwise be what is timed.  At batch 1 the greedy pick runs inside the
-    # decode launch (mk_decode_step_greedy); batched plans, or
-    # --separate-pick, time the decode launch and then mk_greedy_next.
-    # Falls back to direct launches if capture is refused.
-    fused = B == 1 and not args.tensor_cores and not args.separate_pick
+    # otherwise be what is timed.  The greedy pick runs inside the decode
+    # launch (mk_decode_step_greedy); --separate-pick times the decode launch
+    # and then mk_greedy_next.  Falls back to direct launches if capture is
+    # refused.
+    fused = not args.separate_pick
 
     def step_decode():
         if fused:
@@ -558,7 +558,7 @@ def main():
                     help="run the projections as tcgen05 tiles at batch 1 too (default: CUDA-core matvecs)")
     ap.add_argument("--no-graph", action="store_true", help="time direct launches instead of CUDA graph replays")
     ap.add_argument("--separate-pick", action="store_true",
-                    help="batch 1: time the decode launch and mk_greedy_next instead of the fused pick")
+                    help="time the decode launch and mk_greedy_next instead of the pick fused into the decode launch")
     ap.add_argument("--plan-opt", action="append", default=[], metavar="FIELD=INT",
                     help="set an mk_plan_options field (tuning sweeps), e.g. max_inflight=3")
     ap.add_argument("--trace-out", default="", help="write a per-phase task trace of one extra step here")

@@ -47,7 +47,7 @@ def build(force: bool = False) -> Path:
 
 class _Cfg(ctypes.Structure):
     _fields_ = [("n_layers", _i), ("hidden", _i), ("n_q_heads", _i), ("n_kv_heads", _i), ("head_dim", _i),
-                ("ffn_dim", _i), ("vocab", _i), ("rms_eps", _d), ("rope_theta", _d)]
+                ("ffn_dim", _i), ("vocab", _i), ("rms_eps", _d), ("rope_theta", _d), ("kv_bf16", _i)]
 
 
 class _LayerW(ctypes.Structure):
@@ -72,6 +72,8 @@ def lib():
         L.orc_set_num_threads.argtypes = [_i]
         L.orc_bf16.restype = _d
         L.orc_bf16.argtypes = [ctypes.c_uint16]
+        L.orc_round_bf16.restype = _d
+        L.orc_round_bf16.argtypes = [_d]
         L.orc_rmsnorm.argtypes = [_i, _p, _p, _d, _p]
         L.orc_matvec.argtypes = [_i, _i, _p, _p, _p]
         L.orc_rope.argtypes = [_i, _p, _i, _d]
@@ -146,6 +148,11 @@ def bf16_value(bits: int) -> float:
     return float(lib().orc_bf16(bits))
 
 
+def round_bf16(x: float) -> float:
+    """The bf16 value nearest to x (ties to even)."""
+    return float(lib().orc_round_bf16(float(x)))
+
+
 # ---------------------------------------------------------------- decoder
 
 class Model:
@@ -153,13 +160,16 @@ class Model:
 
     ``weights`` is the dict of ``synth.host_weights``.  For models too large
     for host memory, build with ``layers=None`` and drive ``layer_step`` with
-    per-layer weights instead.
+    per-layer weights instead.  ``kv_bf16``: the cache stores every appended
+    key and value rounded to the nearest bf16 (a bf16 KV cache); otherwise it
+    keeps them in fp64.
     """
 
-    def __init__(self, cfg, weights: dict):
+    def __init__(self, cfg, weights: dict, kv_bf16: bool = False):
         self.cfg = cfg
+        self.kv_bf16 = bool(kv_bf16)
         self._c = _Cfg(cfg.n_layers, cfg.hidden, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.ffn_dim,
-                       cfg.vocab, cfg.rms_eps, cfg.rope_theta)
+                       cfg.vocab, cfg.rms_eps, cfg.rope_theta, int(kv_bf16))
         self._keep = []
         self.embed = _u16(weights["embed"])
         self.lm_head = _u16(weights["lm_head"])

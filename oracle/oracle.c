@@ -36,6 +36,9 @@
 typedef struct {
     int n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn_dim, vocab;
     double rms_eps, rope_theta;
+    /* nonzero: the cache stores each appended key and value as the nearest
+     * bf16 value (the decoder's KV cache holds bf16; see orc_round_bf16) */
+    int kv_bf16;
 } orc_cfg;
 
 /* Per-layer weights, bf16 bit patterns, row-major [out][in]. */
@@ -81,6 +84,17 @@ double orc_bf16(uint16_t h) {
     float f;
     memcpy(&f, &u, 4);
     return (double)f;
+}
+
+/* The bf16 value nearest to x, ties to the even significand: bf16 keeps 8
+ * significant bits (1 implicit + 7 stored) over fp32's exponent range, so
+ * for a finite nonzero x with 2^e <= |x| < 2^(e+1) the representable values
+ * near x are the multiples of 2^(e-7).  (Every value here is far inside the
+ * normal range; zeros and non-finite values pass through.) */
+double orc_round_bf16(double x) {
+    if (x == 0.0 || !isfinite(x)) return x;
+    const double step = ldexp(1.0, ilogb(x) - 7);
+    return nearbyint(x / step) * step; /* default rounding mode: to nearest, ties to even */
 }
 
 /* RMSNorm: y_i = g_i * x_i / sqrt(mean_j x_j^2 + eps). */
@@ -170,6 +184,11 @@ int orc_layer_step(const orc_cfg *cfg, const orc_layer_w *w, double *kc, double 
     orc_matvec(nkv * d, H, w->wv, xn, v);
     for (int h = 0; h < nq; ++h) orc_rope(d, q + (size_t)h * d, pos, cfg->rope_theta);
     for (int h = 0; h < nkv; ++h) orc_rope(d, k + (size_t)h * d, pos, cfg->rope_theta);
+    if (cfg->kv_bf16)
+        for (int i = 0; i < nkv * d; ++i) {
+            k[i] = orc_round_bf16(k[i]);
+            v[i] = orc_round_bf16(v[i]);
+        }
     memcpy(kc + (size_t)pos * nkv * d, k, sizeof(double) * nkv * d);
     memcpy(vc + (size_t)pos * nkv * d, v, sizeof(double) * nkv * d);
     for (int h = 0; h < nq; ++h) {
@@ -253,6 +272,11 @@ int orc_full_forward(const orc_cfg *cfg, const orc_weights *w, int n, const int 
             orc_matvec(nkv * d, H, lw->wv, Xn + (size_t)t * H, Vx + (size_t)t * nkv * d);
             for (int h = 0; h < nq; ++h) orc_rope(d, Q + ((size_t)t * nq + h) * d, t, cfg->rope_theta);
             for (int h = 0; h < nkv; ++h) orc_rope(d, Kx + ((size_t)t * nkv + h) * d, t, cfg->rope_theta);
+            if (cfg->kv_bf16)
+                for (int i = 0; i < nkv * d; ++i) {
+                    Kx[(size_t)t * nkv * d + i] = orc_round_bf16(Kx[(size_t)t * nkv * d + i]);
+                    Vx[(size_t)t * nkv * d + i] = orc_round_bf16(Vx[(size_t)t * nkv * d + i]);
+                }
         }
         for (int h = 0; h < nq; ++h) {
             int hk = h / group;

@@ -536,14 +536,10 @@ mk_status mk_decode_step_greedy(mk_plan *p, int32_t *tokens, int32_t *positions,
     if (st != MK_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     KParams k = step_params(p, tokens, 1, positions, 1, kv, logits);
-    if (!p->tables.g.tc) {
-        k.greedy = 1;
-        k.next_tokens = tokens;
-        k.next_positions = positions;
-        return launch_step(p, k, s);
-    }
-    if ((st = launch_step(p, k, s)) != MK_OK) return st;
-    return cuda_status(launch_greedy_next(logits, p->cfg.batch, p->cfg.vocab, tokens, positions, s));
+    k.greedy = 1;
+    k.next_tokens = tokens;
+    k.next_positions = positions;
+    return launch_step(p, k, s);
 }
 
 mk_status mk_decode_step_ablation(mk_plan *p, const int32_t *tokens, const int32_t *positions,

@@ -93,6 +93,7 @@ struct SmemCtl {
     uint32_t tmem_base;
     uint32_t ep_last;             // the epilogue finishes this row tile (last contributor)
     float rs[kTcMaxBatch];        // 1/rms of each sequence's projection input
+    unsigned long long amax_seq[kTcMaxBatch];  // fused greedy pick: this CTA's packed maximum per sequence
     float ssq_red[4][kTcMaxBatch];  // per-epilogue-warp partial sums of x^2
 };
 
@@ -757,6 +758,24 @@ __device__ __forceinline__ float warp_reduce16(const float (&a)[16], int lane) {
     return e;
 }
 
+// Maximum of 16 per-lane 64-bit keys over the warp, scattered: lane l
+// returns the warp maximum of key (l / 2) % 16 (the pattern of warp_reduce16).
+__device__ __forceinline__ unsigned long long warp_max16_u64(const unsigned long long (&a)[16], int lane) {
+    const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4, h2 = lane & 2;
+    auto mx = [](unsigned long long x, unsigned long long y) { return x > y ? x : y; };
+    unsigned long long b[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) b[i] = mx(h16 ? a[i + 8] : a[i], __shfl_xor_sync(0xFFFFFFFFu, h16 ? a[i] : a[i + 8], 16));
+    unsigned long long c4[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c4[i] = mx(h8 ? b[i + 4] : b[i], __shfl_xor_sync(0xFFFFFFFFu, h8 ? b[i] : b[i + 4], 8));
+    unsigned long long d2[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) d2[i] = mx(h4 ? c4[i + 2] : c4[i], __shfl_xor_sync(0xFFFFFFFFu, h4 ? c4[i] : c4[i + 2], 4));
+    unsigned long long e = mx(h2 ? d2[1] : d2[0], __shfl_xor_sync(0xFFFFFFFFu, h2 ? d2[0] : d2[1], 2));
+    return mx(e, __shfl_xor_sync(0xFFFFFFFFu, e, 1));
+}
+
 // acc (two fp32 lanes, even and odd columns) += the 8 bf16 weights of w
 // times x: paired fp32 FMAs (fma.rn.f32x2), one per two weights.  The bf16
 // halves of each 32-bit word are widened exactly (shift, mask).
@@ -1279,6 +1298,7 @@ struct Consumer {
                 float ssum = 0.f;
                 for (int j = 0; j < p.h_tiles; ++j) ssum += __ldcg(p.ssq + (size_t)b * p.h_tiles + j);
                 sc->rs[b] = rsqrtf(ssum / (float)p.H + p.eps);
+                sc->amax_seq[b] = 0ull;
             }
         }
         epi_bar();
@@ -1327,6 +1347,13 @@ struct Consumer {
             tc_fence_before();
             epi_bar();
             if (et == 0) mbar_arrive(&sc->acc_empty[ab]);
+        }
+        if (op == OP_LM && p.greedy) {
+            // fused greedy pick: this CTA's best (logit, row) of every sequence,
+            // one 64-bit max per sequence; the last CTA out writes the tokens
+            for (int b = et; b < p.B; b += kEpiThreads)
+                if (sc->amax_seq[b] != 0ull)
+                    atomicMax(reinterpret_cast<unsigned long long *>(p.ctl + p.cl.amax_idx) + b, sc->amax_seq[b]);
         }
     }
 
@@ -1420,6 +1447,15 @@ struct Consumer {
                 // per-warp sums of x^2 for the 16 sequences of this chunk
                 const float s16 = warp_reduce16(sq, lane);
                 if ((lane & 1) == 0) sc->ssq_red[q4][c0 + ((lane >> 1) & 15)] = s16;
+            }
+            if (op == OP_LM && p.greedy) {
+                // this warp's best (logit, row) of each of the chunk's 16 sequences
+                unsigned long long key[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    key[i] = (c0 + i < p.B && row_ok) ? pack_logit(sc->rs[c0 + i] * v[0][i], orow) : 0ull;
+                const unsigned long long k16 = warp_max16_u64(key, lane);
+                if ((lane & 1) == 0 && k16 != 0ull) atomicMax(&sc->amax_seq[c0 + ((lane >> 1) & 15)], k16);
             }
         }
         if (op == OP_O || op == OP_DOWN) {
@@ -2032,12 +2068,14 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant_
             for (int i = 0; i < p.cl.n_events + p.cl.n_done; ++i) p.ctl[i] = 0u;
             *ex = 0u;
             if (p.greedy && !p.skip_lm && (p.only_op < 0 || p.only_op == OP_LM) && !global_abort(p)) {
-                // fused greedy pick (batch 1): every CTA's maximum is in
+                // fused greedy pick: every CTA's maximum is in
                 unsigned long long *am = reinterpret_cast<unsigned long long *>(p.ctl + p.cl.amax_idx);
-                const unsigned long long w = __ldcg(am);
-                p.next_tokens[0] = (w == 0ull) ? 0x7FFFFFFF : (int32_t)(0xFFFFFFFFu - (uint32_t)w);
-                p.next_positions[0] += 1;
-                *am = 0ull;
+                for (int b = 0; b < p.B; ++b) {
+                    const unsigned long long w = __ldcg(am + b);
+                    p.next_tokens[b] = (w == 0ull) ? 0x7FFFFFFF : (int32_t)(0xFFFFFFFFu - (uint32_t)w);
+                    p.next_positions[b] += 1;
+                    am[b] = 0ull;
+                }
             }
             __threadfence();
         }

@@ -47,15 +47,16 @@ def gpu_plan(m, max_seq: int, batch: int = 1, seed: int = 0, opts=None, kv_shuff
 _MODELS: dict = {}
 
 
-def oracle_model(m, seed: int = 0) -> oracle.Model:
+def oracle_model(m, seed: int = 0, kv_bf16: bool = False) -> oracle.Model:
     """Host weights are generated once per (shape, seed) and kept (the
-    8B-shaped ones take 16 GB)."""
+    8B-shaped ones take 16 GB).  kv_bf16: the oracle's cache stores its keys
+    and values rounded to bf16, as the GPU's paged cache does."""
     key = (m, seed)
     if key not in _MODELS:
         if len(_MODELS) >= 2:
             _MODELS.pop(next(iter(_MODELS)))
-        _MODELS[key] = oracle.Model(m, synth.host_weights(m, seed))
-    return _MODELS[key]
+        _MODELS[key] = synth.host_weights(m, seed)
+    return oracle.Model(m, _MODELS[key], kv_bf16=kv_bf16)
 
 
 def run_teacher_forced(plan: mk.Plan, kv: mk.KVCache, model: oracle.Model, prompt: np.ndarray, steps: int,

@@ -42,6 +42,11 @@ MUTANTS = [
     ("mask leaks next token", "if (j > i) {", "if (j > i + 1) {"),
     ("mlp norm uses attention gain", "orc_rmsnorm(H, x, w->mlp_norm, cfg->rms_eps, xn);",
      "orc_rmsnorm(H, x, w->attn_norm, cfg->rms_eps, xn);"),
+    ("bf16 rounding keeps 9 bits", "ldexp(1.0, ilogb(x) - 7)", "ldexp(1.0, ilogb(x) - 8)"),
+    ("bf16 cache leaves values unrounded", "            v[i] = orc_round_bf16(v[i]);", "            v[i] = v[i];"),
+    ("full forward rounds keys only",
+     "Vx[(size_t)t * nkv * d + i] = orc_round_bf16(Vx[(size_t)t * nkv * d + i]);",
+     "Vx[(size_t)t * nkv * d + i] = Vx[(size_t)t * nkv * d + i];"),
 ]
 
 

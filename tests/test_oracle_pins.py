@@ -255,6 +255,49 @@ def test_decode_equals_full_causal_forward():
         assert np.allclose(step, full[p], rtol=1e-11, atol=1e-12), f"position {p}"
 
 
+def test_round_bf16_matches_fp32_round_to_nearest_even():
+    """For values exactly representable in fp32, the nearest bf16 is fp32's
+    top 16 bits rounded to nearest, ties to even: written here as integer bit
+    manipulation, independent of the oracle's arithmetic on doubles."""
+    r = rng(3)
+    x = (r.standard_normal(20000) * 2.0 ** r.integers(-30, 30, 20000)).astype(np.float32)
+    u = x.view(np.uint32).astype(np.uint64)
+    want = (((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16).astype(np.uint32).view(np.float32).astype(np.float64)
+    got = np.array([oracle.round_bf16(float(v)) for v in x])
+    assert np.array_equal(got, want)
+    # ties: 1 + 2^-8 is half way between 1 and 1 + 2^-7 (odd significand) -> 1;
+    # 1 + 3 * 2^-8 is half way between 1 + 2^-7 and 1 + 2^-6 (even) -> 1 + 2^-6
+    assert oracle.round_bf16(1 + 2 ** -8) == 1.0 and oracle.round_bf16(-(1 + 2 ** -8)) == -1.0
+    assert oracle.round_bf16(1 + 3 * 2 ** -8) == 1 + 2 ** -6
+    for v in (0.0, 1.0, -2.5, 2.0 ** -100, 3.0 * 2 ** 60):
+        assert oracle.round_bf16(v) == v
+    assert all(oracle.round_bf16(g) == g for g in got[:200])  # idempotent
+
+
+def _is_bf16(a):
+    a32 = np.asarray(a, dtype=np.float64).astype(np.float32)
+    return np.array_equal(a32.astype(np.float64), np.asarray(a)) and not np.any(a32.view(np.uint32) & 0xFFFF)
+
+
+def test_bf16_cache_holds_bf16_values_and_decode_equals_full_forward():
+    """With a bf16 KV cache every stored key and value is a bf16 value, and
+    token-by-token decode still equals the full causal forward, which rounds
+    its keys and values in a separate code path; the rounding moves the
+    logits, but only by a rounding-sized amount."""
+    w = synth.host_weights(TINY_T, 0)
+    m = oracle.Model(TINY_T, w, kv_bf16=True)
+    toks = synth.tokens(12, 0, 2, TINY_T.vocab)
+    full = m.full_forward(toks)
+    kc, vc = m.new_cache(16)
+    for p, t in enumerate(toks):
+        step = m.decode_step(kc, vc, int(t), p)
+        assert np.allclose(step, full[p], rtol=1e-11, atol=1e-12), f"position {p}"
+    assert _is_bf16(kc[:, :12]) and _is_bf16(vc[:, :12])
+    plain = oracle.Model(TINY_T, w).full_forward(toks)
+    assert not np.allclose(full, plain, rtol=0, atol=1e-9)
+    assert np.linalg.norm(full - plain) / np.linalg.norm(plain) < 1e-2
+
+
 def test_full_forward_is_causal():
     m, _ = _model(TINY_T)
     toks = synth.tokens(10, 0, 1, TINY_T.vocab)
