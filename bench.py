@@ -318,6 +318,37 @@ def seeded_context(wl) -> bool:
     return wl.prompt_len >= 1024
 
 
+def time_prefill(mk, plan, m, weights, B, max_seq, prompt_d, kv, logits, reps, popts):
+    """Prompt prefill timed with CUDA events: the plan's mk_prefill (the
+    chunked-prefill engine below 64 sequences), then the decode step once
+    per position (a plan with prefill_by_decode) on the same cache.  Both
+    rewrite the same K/V values the first prefill wrote."""
+    import torch
+
+    stream = torch.cuda.current_stream()
+    T = prompt_d.shape[-1]
+
+    def timed(p):
+        p.prefill(prompt_d, kv, logits)  # warm-up (the engine exists already)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            p.prefill(prompt_d, kv, logits)
+        b.record(stream)
+        torch.cuda.synchronize()
+        p.check()
+        return a.elapsed_time(b) / reps
+
+    ms = timed(plan)
+    kw = {f: getattr(popts, f) for f, _ in popts._fields_ if f != "reserved"} if popts is not None else {}
+    ref = mk.Plan(m, weights, batch=B, max_seq=max_seq, opts=mk.mk_plan_options(**{**kw, "prefill_by_decode": 1}))
+    ms_dec = timed(ref)
+    ref.close()
+    return {"tokens": int(T * B), "ms": ms, "tokens_per_s": T * B / ms * 1e3,
+            "engine": "chunked (64 tokens per launch)" if B < 64 else "decode step per position",
+            "by_decode_ms": ms_dec, "by_decode_tokens_per_s": T * B / ms_dec * 1e3}
+
+
 def run_mk(args, wl):
     import torch
 
@@ -341,6 +372,7 @@ def run_mk(args, wl):
     kv = mk.KVCache(m, B, max_seq, shuffle_seed=1, device=dev)
     logits = torch.empty((B, m.vocab), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    prefill_info = None
     tok = torch.empty(B, dtype=torch.int32, device=dev)
     pos = torch.full((B,), wl.prompt_len - 1, dtype=torch.int32, device=dev)
     if seeded_context(wl):
@@ -355,8 +387,12 @@ def run_mk(args, wl):
         pos.fill_(wl.prompt_len)
     else:
         prompt = np.stack([synth.tokens(wl.prompt_len, wl.seed, b, m.vocab) for b in range(B)])
-        plan.prefill(torch.tensor(prompt, dtype=torch.int32, device=dev), kv, logits)
+        prompt_d = torch.tensor(prompt, dtype=torch.int32, device=dev)
+        plan.prefill(prompt_d, kv, logits)
         plan.greedy_next(logits, tok, pos)  # first generated token, at position prompt_len
+        if args.prefill_reps > 0:
+            prefill_info = time_prefill(mk, plan, m, weights, B, max_seq, prompt_d, kv, logits, args.prefill_reps,
+                                        popts)
     for _ in range(args.warmup):
         plan.decode_step(tok, pos, kv, logits)
         plan.greedy_next(logits, tok, pos)
@@ -448,6 +484,8 @@ def run_mk(args, wl):
 
     for _ in range(args.warmup):  # first-call costs stay out of the timed region, as for `value`
         e2e_step()
+    # the same context lengths as the device-timed steps (their cache slots are rewritten)
+    n_pos[:] = ctx0 - 1
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(args.e2e_steps):
@@ -531,6 +569,7 @@ def run_mk(args, wl):
                     "d2h_bytes_per_step": 4 * B * m.vocab},
             "gpu_launches": (1 if fused else 2) * args.steps,
             "ablation": abl,
+            "prefill": prefill_info,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -548,6 +587,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=32)
     ap.add_argument("--ablation-steps", type=int, default=8)
     ap.add_argument("--cpu-samples", type=int, default=8, help="whole oracle decode steps timed on all host cores")
+    ap.add_argument("--prefill-reps", type=int, default=3, help="prompt prefills timed (0: skip)")
     ap.add_argument("--cpu-single-thread-steps", type=int, default=1,
                     help="whole oracle decode steps timed on one host thread (0: skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -116,7 +116,14 @@ typedef struct {
                               batch >= 2; 1: tcgen05 tiles at every batch */
     int32_t max_inflight;  /* ring copies a CTA keeps in flight at once (default: 2 at batch 1,
                               every free ring slot when batched; >= num_slots: no cap) */
-    int32_t reserved[5];
+    int32_t kv_append;     /* 1: a task of its own (op 8) RoPEs and appends every row's new K/V
+                              to the cache before attention, which then reads the new token from
+                              the cache like the rest; rows may then be consecutive tokens of one
+                              sequence (the chunked-prefill graph of mk_prefill).  Default 0: the
+                              last attention split appends its row's K/V itself */
+    int32_t prefill_by_decode; /* 1: mk_prefill runs the decode step once per position instead of
+                                  the chunked-prefill engine */
+    int32_t reserved[3];
 } mk_plan_options;
 
 typedef struct mk_plan mk_plan; /* opaque, library-owned */
@@ -171,11 +178,19 @@ mk_status mk_decode_step_host(mk_plan *plan, const int32_t *tokens_host, const i
 
 /* Passage: the prompt phase before decoding ("Compilar LLM en un
  * MegaKernel…", "Valor central de MPK": a 39-token prompt, then 512 decode
- * steps).
+ * steps), and the comparison of small-batch decode with large-batch prefill
+ * of "Cómo la fusión de kernels CUDA acelera…", "Comprueba si la fusión ha
+ * ayudado".
  * Prefill T prompt tokens per sequence (device int32 [batch][T]) at
- * positions 0..T-1 by running the decode step once per position; writes the
- * logits of position T-1 (device fp32 [batch][vocab]).  The LM head runs only
- * for the last position. */
+ * positions 0..T-1; writes the logits of position T-1 (device fp32
+ * [batch][vocab]); the LM head runs only for the last chunk or position.
+ * Plans of fewer than 64 sequences use a chunked-prefill engine: up to 64
+ * consecutive tokens of one sequence per persistent launch, as the rows of
+ * the tensor-core path, with a task that appends every row's K/V to the cache
+ * before the rows attend (causally) to it.  The engine is a second plan of
+ * the same weights, made (allocating device memory) on the first call;
+ * options.prefill_by_decode, or a failure to make it, selects the decode
+ * step once per position instead, as batched plans always do. */
 mk_status mk_prefill(mk_plan *plan, const int32_t *tokens, int32_t T, const mk_kv_cache *kv, float *last_logits,
                      void *stream);
 
@@ -274,7 +289,8 @@ void mk_plan_destroy(mk_plan *plan);
  * --------------------------------------------------------------------- */
 typedef struct {
     int32_t cta;         /* worker CTA whose queue holds the task */
-    int32_t op;          /* 1 QKV, 2 ATTN, 3 O, 4 GATE_UP, 5 DOWN, 6 LM_HEAD, 7 EMBED (batched only) */
+    int32_t op;          /* 1 QKV, 2 ATTN, 3 O, 4 GATE_UP, 5 DOWN, 6 LM_HEAD, 7 EMBED (batched only),
+                            8 KV_APPEND (kv_append graphs only) */
     int32_t layer;
     int32_t wait_event;  /* -1: none */
     int32_t wait_count;  /* proceed when counter[wait_event] >= wait_count */

@@ -13,7 +13,7 @@ import ctypes
 from .build import LIB, build
 
 MK_OK, MK_ERR_INVALID, MK_ERR_CUDA, MK_ERR_LAUNCH, MK_ERR_TIMEOUT, MK_ERR_BOUNDS, MK_ERR_OOM, MK_ERR_UNSUPPORTED = range(8)
-OP_QKV, OP_ATTN, OP_O, OP_GU, OP_DOWN, OP_LM, OP_EMBED = range(1, 8)
+OP_QKV, OP_ATTN, OP_O, OP_GU, OP_DOWN, OP_LM, OP_EMBED, OP_KVA = range(1, 9)
 TC_TILE_M, TC_TILE_K = 128, 64  # batched path: weight rows x columns per unit
 
 _i32, _f32, _vp = ctypes.c_int32, ctypes.c_float, ctypes.c_void_p
@@ -43,7 +43,7 @@ class mk_plan_options(ctypes.Structure):
     _fields_ = [("num_ctas", _i32), ("attn_splits", _i32), ("slot_bytes", _i32), ("num_slots", _i32),
                 ("timeout_ms", _i32), ("planner_seed", ctypes.c_uint32), ("l2_prefetch_kb", _i32),
                 ("test_unreachable_event", _i32), ("trace", _i32), ("tensor_cores", _i32), ("max_inflight", _i32),
-                ("reserved", _i32 * 5)]
+                ("kv_append", _i32), ("prefill_by_decode", _i32), ("reserved", _i32 * 3)]
 
 
 class mk_device_error(ctypes.Structure):

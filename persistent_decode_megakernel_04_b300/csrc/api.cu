@@ -45,6 +45,14 @@ struct mk_plan {
     uint8_t *d_tmaps = nullptr;
     uint8_t *d_down_maps = nullptr;  // batch 1: per-layer w_down tensor maps
     KParams base{};
+    // host copies of the weight pointers (the chunked-prefill engine's plan reuses them)
+    std::vector<LayerW> hlw;
+    const void *w_embed = nullptr, *w_lm = nullptr, *w_final = nullptr;
+    // chunked-prefill engine, made on first use: a kv-append plan whose
+    // kPrefillRows batch rows are consecutive tokens of one sequence
+    mk_plan *pre = nullptr;
+    float *d_pre_logits = nullptr;  // [kPrefillRows][vocab]
+    int32_t *d_pre_tok = nullptr, *d_pre_pos = nullptr;
     // tensor maps of the last KV cache seen (encoded once per cache, not per step)
     mk_kv_cache kv_seen{};
     bool kv_maps_valid = false;
@@ -171,6 +179,7 @@ mk_status cuda_status(cudaError_t e) {
 }
 
 void free_plan(mk_plan *p) {
+    if (p->pre) free_plan(p->pre);
     if (p->h_err) cudaFreeHost(p->h_err);
     for (void *q : p->allocs) cudaFree(q);
     p->allocs.clear();
@@ -186,6 +195,7 @@ KParams step_params(const mk_plan *p, const int32_t *tokens, int32_t tok_stride,
     k.page_table = kv->page_table;
     k.num_pages = kv->num_pages;
     k.max_pages = kv->max_pages_per_seq;
+    k.pt_stride = kv->max_pages_per_seq;
     k.tokens = tokens;
     k.tok_stride = tok_stride;
     k.positions = positions;
@@ -392,7 +402,11 @@ mk_status mk_plan_create_ex(const mk_model_cfg *cfg, const mk_weight_ptrs *w, co
         }
     }
 
-    std::vector<LayerW> lw(c.n_layers);
+    p->w_embed = w->embed;
+    p->w_lm = w->lm_head;
+    p->w_final = w->final_norm;
+    std::vector<LayerW> &lw = p->hlw;
+    lw.resize(c.n_layers);
     for (int l = 0; l < c.n_layers; ++l) {
         lw[l].attn_norm = static_cast<const uint16_t *>(w->attn_norm[l]);
         lw[l].wq = static_cast<const uint16_t *>(w->wq[l]);
@@ -489,6 +503,7 @@ mk_status mk_plan_create_ex(const mk_model_cfg *cfg, const mk_weight_ptrs *w, co
     k.only_op = -1;
     k.only_layer = -1;
     k.skip_lm = 0;
+    k.kv_appended = g.kv_append ? 1 : 0;
     k.timeout_ns = (uint64_t)p->opt.timeout_ms * 1000000ull;
     k.trace = p->d_trace;
     k.trace_stride = p->trace_stride;
@@ -570,12 +585,95 @@ mk_status mk_decode_step_ablation(mk_plan *p, const int32_t *tokens, const int32
     return cuda_status(launch_megakernel(k, p->variant, p->tables.g.num_ctas, p->smem, false, s));
 }
 
+}  // extern "C"
+
+namespace {
+
+// Rows of one chunked-prefill launch.
+constexpr int32_t kPrefillRows = 64;
+
+// The chunked-prefill engine of a plan: a plan of the same decoder whose
+// kPrefillRows batch rows are consecutive tokens of one sequence, run on the
+// tensor-core path with the kv-append graph (every row's K/V is in the cache
+// before any row attends).  Made on first use.
+mk_status ensure_prefill_engine(mk_plan *p) {
+    if (p->pre) return MK_OK;
+    mk_model_cfg c = p->cfg;
+    c.batch = kPrefillRows;
+    mk_plan_options o;
+    std::memset(&o, 0, sizeof(o));
+    o.num_ctas = p->opt.num_ctas;
+    o.timeout_ms = p->opt.timeout_ms;
+    o.tensor_cores = 1;
+    o.kv_append = 1;
+    const int L = c.n_layers;
+    std::vector<const void *> f[9];
+    for (auto &v : f) v.resize(L);
+    for (int l = 0; l < L; ++l) {
+        const LayerW &w = p->hlw[l];
+        const void *ptrs[9] = {w.attn_norm, w.wq, w.wk, w.wv, w.wo, w.mlp_norm, w.w_gate, w.w_up, w.w_down};
+        for (int i = 0; i < 9; ++i) f[i][l] = ptrs[i];
+    }
+    const mk_weight_ptrs w = {p->w_embed, p->w_lm, p->w_final, f[0].data(), f[1].data(), f[2].data(), f[3].data(),
+                              f[4].data(), f[5].data(), f[6].data(), f[7].data(), f[8].data()};
+    mk_plan *q = nullptr;
+    mk_status st = mk_plan_create_ex(&c, &w, &o, &q);
+    if (st != MK_OK) return st;
+    if ((st = dev_alloc(q, &p->d_pre_logits, (size_t)kPrefillRows * c.vocab)) != MK_OK ||
+        (st = dev_alloc(q, &p->d_pre_tok, kPrefillRows)) != MK_OK ||
+        (st = dev_alloc(q, &p->d_pre_pos, kPrefillRows)) != MK_OK) {
+        free_plan(q);
+        return st;
+    }
+    p->pre = q;
+    return MK_OK;
+}
+
+// Prefill of every sequence's T tokens through the engine: chunks of up to
+// kPrefillRows consecutive tokens, one launch each (the rows past a short
+// last chunk repeat its last token at its position: they write the same K/V
+// to the same slot and are not read); the LM head runs on the last chunk only.
+mk_status prefill_chunked(mk_plan *p, const int32_t *tokens, int32_t T, const mk_kv_cache *kv, float *last_logits,
+                          cudaStream_t s) {
+    mk_plan *q = p->pre;
+    mk_status st = check_kv(q, kv);
+    if (st != MK_OK) return st;
+    const int32_t V = p->cfg.vocab;
+    for (int32_t b = 0; b < p->cfg.batch; ++b) {
+        int32_t n = 0;
+        for (int32_t c0 = 0; c0 < T; c0 += kPrefillRows) {
+            n = std::min(kPrefillRows, T - c0);
+            cudaError_t e = launch_prefill_rows(tokens + (int64_t)b * T + c0, n, c0, kPrefillRows, p->d_pre_tok,
+                                                p->d_pre_pos, s);
+            if (e != cudaSuccess) return cuda_status(e);
+            KParams k = step_params(q, p->d_pre_tok, 1, p->d_pre_pos, 1, kv, p->d_pre_logits);
+            k.page_table = kv->page_table + (int64_t)b * kv->max_pages_per_seq;
+            k.pt_stride = 0;  // every row is a token of sequence b
+            k.skip_lm = (c0 + n < T) ? 1 : 0;
+            if ((st = launch_step(q, k, s)) != MK_OK) return st;
+        }
+        const cudaError_t e = cudaMemcpyAsync(last_logits + (int64_t)b * V, p->d_pre_logits + (int64_t)(n - 1) * V,
+                                              (size_t)V * sizeof(float), cudaMemcpyDeviceToDevice, s);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    return MK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 mk_status mk_prefill(mk_plan *p, const int32_t *tokens, int32_t T, const mk_kv_cache *kv, float *last_logits,
                      void *stream) {
     if (!p || !tokens || !last_logits || T <= 0 || T > p->cfg.max_seq) return MK_ERR_INVALID;
     mk_status st = check_kv(p, kv);
     if (st != MK_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // chunked prefill when a launch of kPrefillRows tokens of one sequence
+    // beats a launch of one token of each sequence
+    if (T > 1 && p->cfg.batch < kPrefillRows && p->opt.prefill_by_decode == 0 &&
+        ensure_prefill_engine(p) == MK_OK)
+        return prefill_chunked(p, tokens, T, kv, last_logits, s);
     for (int32_t t = 0; t < T; ++t) {
         KParams k = step_params(p, tokens + t, T, p->d_iota + t, 0, kv, last_logits);
         k.skip_lm = (t + 1 < T) ? 1 : 0;

@@ -285,32 +285,36 @@ __device__ __forceinline__ const uint16_t *mv_matrix(const KParams &p, int op, c
 
 struct AttnRange {
     int32_t pos;       // position of the new token
-    int32_t blo, bhi;  // 64-token blocks [blo, bhi) of the cached context [0, pos)
-    bool has_new;      // this split also attends to the new token
+    int32_t ctx;       // positions read from the cache: [0, ctx)
+    int32_t blo, bhi;  // 64-token blocks [blo, bhi) of [0, ctx)
+    bool has_new;      // this split also attends to the new token, from registers
     int32_t n_live;    // splits of this (sequence, kv head) with any work
 };
 
-// The cached context [0, pos) is cut into aligned 64-token blocks, and split
-// s of S takes blocks [s*nb/S, (s+1)*nb/S); the last split also handles the
-// new token at pos, which is not read from the cache.
+// The cached context [0, ctx) is cut into aligned 64-token blocks, and split
+// s of S takes blocks [s*nb/S, (s+1)*nb/S).  ctx = pos when the last split
+// handles the new token at pos itself (not read from the cache); ctx =
+// pos + 1 in kv-append graphs, where OP_KVA put it in the cache first.
 __device__ __forceinline__ AttnRange attn_range(const KParams &p, const Task &t) {
     AttnRange r;
     r.pos = p.positions[(int64_t)t.a0 * p.pos_stride];
-    const int64_t nb = (r.pos + kAttnBlock - 1) / kAttnBlock;
+    r.ctx = p.kv_appended ? r.pos + 1 : r.pos;
+    const int64_t nb = (r.ctx + kAttnBlock - 1) / kAttnBlock;
     r.blo = (int32_t)((int64_t)t.a2 * nb / t.a3);
     r.bhi = (int32_t)((int64_t)(t.a2 + 1) * nb / t.a3);
-    r.has_new = (t.a2 == t.a3 - 1);
+    r.has_new = !p.kv_appended && (t.a2 == t.a3 - 1);
     // nb <= S blocks land on nb distinct splits (the last one among them);
     // with no cached block only the new token's split works
     r.n_live = nb < 1 ? 1 : (nb < t.a3 ? (int32_t)nb : t.a3);
     return r;
 }
 
-// The j-th of the r.n_live splits with work (cached blocks, or the new
-// token: the last split).  With nb <= S blocks, block j is the only block of
-// split ((j + 1) S - 1) / nb; with more blocks every split has some.
-__device__ __forceinline__ int32_t live_split(int32_t pos, int32_t j, int32_t S) {
-    const int64_t nb = (pos + kAttnBlock - 1) / kAttnBlock;
+// The j-th of the n_live splits with work over a cached context of ctx
+// positions (cached blocks, or the new token: the last split).  With nb <= S
+// blocks, block j is the only block of split ((j + 1) S - 1) / nb; with more
+// blocks every split has some.
+__device__ __forceinline__ int32_t live_split(int32_t ctx, int32_t j, int32_t S) {
+    const int64_t nb = (ctx + kAttnBlock - 1) / kAttnBlock;
     if (nb == 0) return S - 1;
     if (nb > S) return j;
     return (int32_t)(((int64_t)(j + 1) * S - 1) / nb);
@@ -521,7 +525,7 @@ struct Producer {
         const KParams &p = *c.p;
         const AttnRange r = attn_range(p, t);
         const int ts = p.attn_ts, halves = p.d / 64;
-        const int32_t *pt = p.page_table + (int64_t)t.a0 * p.max_pages;
+        const int32_t *pt = p.page_table + (int64_t)t.a0 * p.pt_stride;
         for (int32_t blk = r.blo; blk < r.bhi; ++blk) {
             const int32_t tok0 = blk * kAttnBlock;
             const int32_t pg = pt[tok0 / p.page_size];
@@ -564,6 +568,28 @@ struct Producer {
         return true;
     }
 
+    // Kv-append graphs: the cache blocks an attention task reads include
+    // positions that OP_KVA tasks write in this launch, so their copies wait
+    // until the scheduler has seen the task's event (queue position i
+    // released), then order those generic-proxy writes before the TMA reads.
+    __device__ bool wait_released(const Ctx &c, int i) {
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t it = 1;; ++it) {
+            const uint32_t r = ld_acquire_cta(&c.sc->ready);
+            if (r == kReadyAbort) return false;
+            if (r >= (uint32_t)(i + 1)) break;
+            if ((it & 63u) == 0) {
+                if (local_abort(c)) return false;
+                if (globaltimer_ns() - t0 > 4 * c.p->timeout_ns) {
+                    record_error(c, 4 /*MK_ERR_TIMEOUT*/, SITE_READY_WAIT, i);
+                    return false;
+                }
+            }
+        }
+        fence_proxy_async_global();
+        return true;
+    }
+
     // Wait for the copies of every slot's most recent page (abort path and
     // normal exit alike), so that no copy is in flight when the CTA exits.
     __device__ void drain(const Ctx &c) {
@@ -597,8 +623,8 @@ __device__ void producer_role(const Ctx &c, const Task *q, int nt) {
         bool ok = true;
         if (t.op == OP_O && !c.p->tc && c.p->l2_prefetch_bytes > 0)
             pr.prefetch_past_attention(c, t, i + 1 < nt ? &q[i + 1] : nullptr);
-        if (t.op == OP_ATTN) ok = pr.run_attn(c, t);
-        else if (t.op == OP_EMBED) ok = true;
+        if (t.op == OP_ATTN) ok = (!c.p->kv_appended || pr.wait_released(c, i)) && pr.run_attn(c, t);
+        else if (t.op == OP_EMBED || t.op == OP_KVA) ok = true;
         else ok = c.p->tc ? pr.run_gemm(c, t) : pr.run_matvec(c, t);
         if (!ok) break;
     }
@@ -1497,6 +1523,32 @@ struct Consumer {
         }
     }
 
+    // ------------------------------------------- kv-append graphs: OP_KVA
+    // Items [a0, a1) = (batch row, kv head): RoPE on the row's new k, both
+    // rounded to bf16 and stored at its position in the paged cache, where
+    // the attention tasks of every row then read it (by TMA: the stores are
+    // fenced for the async proxy).
+    __device__ void run_kva(const Ctx &c, const Task &t) {
+        const KParams &p = *c.p;
+        const int half = p.d / 2;
+        for (int32_t it = t.a0; it < t.a1; ++it) {
+            const int32_t b = it / p.nkv, kvh = it % p.nkv;
+            const int32_t pos = p.positions[(int64_t)b * p.pos_stride];
+            const int32_t page = p.page_table[(int64_t)b * p.pt_stride + pos / p.page_size];
+            const float *kh = p.qkv + (int64_t)b * p.qkv_rows + (int64_t)p.nq * p.d + (int64_t)kvh * p.d;
+            const float *vh = kh + (int64_t)p.nkv * p.d;
+            const int64_t off = kv_offset(p, t.layer, page, kvh, pos % p.page_size);
+            if (ct < half) {
+                const float ka = __ldcg(kh + ct), kb = __ldcg(kh + ct + half);
+                const float2 cs = p.rope[(int64_t)pos * half + ct];
+                p.k_pool[off + ct] = f32_to_bf16_bits(ka * cs.x - kb * cs.y);
+                p.k_pool[off + ct + half] = f32_to_bf16_bits(ka * cs.y + kb * cs.x);
+            }
+            if (ct < p.d) p.v_pool[off + ct] = f32_to_bf16_bits(__ldcg(vh + ct));
+        }
+        fence_proxy_async_global();  // read next by the attention tasks' TMA
+    }
+
     // ---------------------------------------------------- attention task
     // One (sequence, kv head, context split) task.  The G query heads of the
     // kv head are split into bf16 high and low parts (2G MMA columns), so the
@@ -1570,7 +1622,7 @@ struct Consumer {
                 kcs = rope[ct];
             }
             if (ct < d) vv = __ldcg(vh + ct);
-            new_page = p.page_table[(int64_t)b * p.max_pages + r.pos / p.page_size];
+            new_page = p.page_table[(int64_t)b * p.pt_stride + r.pos / p.page_size];
         }
         // RoPE'd, pre-scaled queries of the G heads sharing this kv head, in
         // fp32 and split into bf16 high / low parts (rows G..2G-1 the low parts)
@@ -1671,7 +1723,7 @@ struct Consumer {
                     const int tok = 16 * wc + tr + (i >> 1) * 8;
                     const int head = (G == 1) ? 0 : 2 * cq + (i & 1);
                     const bool live = head_lane && (G != 1 || (i & 1) == 0);
-                    if (live) sc->at.s_s[head][tok] = (tok0 + tok < r.pos) ? v : -INFINITY;
+                    if (live) sc->at.s_s[head][tok] = (tok0 + tok < r.ctx) ? v : -INFINITY;
                 }
             }
             compute_bar();
@@ -1857,7 +1909,7 @@ struct Consumer {
                     const int j = j0 + lane;
                     float ms = -INFINITY, ls = 0.f;
                     if (j < r.n_live) {
-                        const float *src = p.attn_part + (pbase + (int64_t)live_split(r.pos, j, S) * G + g) * (d + 2);
+                        const float *src = p.attn_part + (pbase + (int64_t)live_split(r.ctx, j, S) * G + g) * (d + 2);
                         const float2 ml = __ldcg(reinterpret_cast<const float2 *>(src + d));
                         ms = ml.x;
                         ls = ml.y;
@@ -1892,7 +1944,7 @@ struct Consumer {
 #pragma unroll
                         for (int j = 0; j < kChunk; ++j)
                             v[j] = (j0 + j < r.n_live)
-                                       ? __ldcg(reinterpret_cast<const float2 *>(src + live_split(r.pos, j0 + j, S) * sstride))
+                                       ? __ldcg(reinterpret_cast<const float2 *>(src + live_split(r.ctx, j0 + j, S) * sstride))
                                        : make_float2(0.f, 0.f);
 #pragma unroll
                         for (int j = 0; j < kChunk; ++j) {
@@ -1954,6 +2006,7 @@ __device__ void compute_role(const Ctx &c, const Task *q, int nt) {
         if (tr) tr[1] = globaltimer_ns();
         if (t.op == OP_ATTN) cs.run_attn(c, t);
         else if (t.op == OP_EMBED) cs.run_embed(c, t);
+        else if (t.op == OP_KVA) cs.run_kva(c, t);
         else if (p.tc) cs.run_gemm(c, t);
         else cs.run_matvec(c, t);
         // batched path: outputs are read by other CTAs' TMA (async proxy)
@@ -2028,7 +2081,7 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant_
                 continue;
             }
             for (int32_t j = 0; j <= pos / p.page_size; ++j) {
-                const int32_t pg = p.page_table[(int64_t)b * p.max_pages + j];
+                const int32_t pg = p.page_table[(int64_t)b * p.pt_stride + j];
                 if (pg < 0 || pg >= p.num_pages) {
                     record_error(c, 5, SITE_PAGE, pg);
                     break;
@@ -2132,6 +2185,16 @@ __global__ void greedy_next_kernel(const float *logits, int32_t V, int32_t *toke
     }
 }
 
+__global__ void prefill_rows_kernel(const int32_t *src, int32_t n, int32_t p0, int32_t rows, int32_t *tok,
+                                    int32_t *pos) {
+    const int32_t j = threadIdx.x;
+    if (j < rows) {
+        const int32_t jj = j < n ? j : n - 1;
+        tok[j] = src[jj];
+        pos[j] = p0 + jj;
+    }
+}
+
 template <int MAXCH>
 const void *kernel_ptr() {
     return reinterpret_cast<const void *>(&megakernel<MAXCH>);
@@ -2184,6 +2247,17 @@ cudaError_t launch_rope_table(float2 *rope, int32_t max_seq, int32_t d, float th
 cudaError_t launch_greedy_next(const float *logits, int32_t B, int32_t V, int32_t *tokens, int32_t *positions,
                                cudaStream_t stream) {
     greedy_next_kernel<<<B, 1024, 0, stream>>>(logits, V, tokens, positions);
+    return cudaGetLastError();
+}
+
+}  // namespace mk
+
+namespace mk {
+
+cudaError_t launch_prefill_rows(const int32_t *src, int32_t n, int32_t p0, int32_t rows, int32_t *tok, int32_t *pos,
+                                cudaStream_t stream) {
+    if (n < 1 || rows < 1 || rows > 1024) return cudaErrorInvalidValue;
+    prefill_rows_kernel<<<1, rows, 0, stream>>>(src, n, p0, rows, tok, pos);
     return cudaGetLastError();
 }
 

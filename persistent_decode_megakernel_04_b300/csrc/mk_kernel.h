@@ -39,6 +39,8 @@ struct KParams {
     uint16_t *k_pool, *v_pool;
     const int32_t *page_table;
     int32_t num_pages, max_pages;
+    int32_t pt_stride;     // page-table entries between batch rows (0: every row is one sequence)
+    int32_t kv_appended;   // OP_KVA tasks append the new K/V; attention reads positions 0..pos from the cache
     // inputs / outputs of this step
     const int32_t *tokens;
     int32_t tok_stride;
@@ -123,5 +125,10 @@ bool encode_down_map(void *m, const void *w_down, const MvGeom &g);
 cudaError_t launch_rope_table(float2 *rope, int32_t max_seq, int32_t d, float theta, cudaStream_t stream);
 cudaError_t launch_greedy_next(const float *logits, int32_t B, int32_t V, int32_t *tokens, int32_t *positions,
                                cudaStream_t stream);
+
+// Rows of one chunked-prefill launch: tok[j] = src[min(j, n-1)] and
+// pos[j] = p0 + min(j, n-1) for j < rows.
+cudaError_t launch_prefill_rows(const int32_t *src, int32_t n, int32_t p0, int32_t rows, int32_t *tok, int32_t *pos,
+                                cudaStream_t stream);
 
 }  // namespace mk

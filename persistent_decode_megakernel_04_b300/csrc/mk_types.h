@@ -9,7 +9,8 @@ namespace mk {
 enum Op : uint8_t {
     OP_NONE = 0, OP_QKV = 1, OP_ATTN = 2, OP_O = 3, OP_GU = 4, OP_DOWN = 5, OP_LM = 6,
     OP_EMBED = 7,  // batched path only: embedding rows + first RMSNorm statistics
-    OP_COUNT = 8
+    OP_KVA = 8,    // kv-append graphs only: RoPE + bf16 append of every row's new K/V before attention
+    OP_COUNT = 9
 };
 
 constexpr uint16_t kNoEvent = 0xFFFF;

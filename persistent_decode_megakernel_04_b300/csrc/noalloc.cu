@@ -230,6 +230,7 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_model_cfg *cfg, const mk_we
     k.page_table = kv->page_table;
     k.num_pages = kv->num_pages;
     k.max_pages = kv->max_pages_per_seq;
+    k.pt_stride = kv->max_pages_per_seq;
     k.tokens = tokens;
     k.tok_stride = 1;
     k.positions = positions;

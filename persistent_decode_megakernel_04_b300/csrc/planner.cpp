@@ -66,7 +66,7 @@ mk_status check_cfg(const mk_model_cfg &c) {
     if (!(c.rms_eps >= 0.0f) || !(c.rope_theta > 0.0f)) return MK_ERR_INVALID;
     // 16-byte copies need every row length to be a multiple of 8 bf16
     if (c.hidden % 8 || c.ffn_dim % 8 || c.head_dim % 64) return MK_ERR_UNSUPPORTED;
-    if (c.n_layers * 5 + 1 >= 0xFFFF) return MK_ERR_UNSUPPORTED;
+    if (c.n_layers * 6 + 1 >= 0xFFFF) return MK_ERR_UNSUPPORTED;
     const int32_t group = c.n_q_heads / c.n_kv_heads;
     if (group > 8 || (group & (group - 1)) || c.head_dim > 128) return MK_ERR_UNSUPPORTED;
     if (c.page_size % 64) return MK_ERR_UNSUPPORTED;  // attention reads aligned 64-token blocks of a page
@@ -131,7 +131,9 @@ mk_status build_plan(const mk_model_cfg &cfg, const mk_plan_options &opt, PlanTa
     // KV tokens per ring slot: a 64-token attention block fills 1 or 2 slots
     g.tps = (g.slot_bytes >= 2 * d * 2 * 64) ? 64 : 32;
     if (g.slot_bytes < 2 * d * 2 * 32) return MK_ERR_INVALID;
-    g.n_events = 5 * L + (tc ? 1 : 0);
+    const int32_t per = opt.kv_append ? 6 : 5;  // events per layer
+    g.kv_append = opt.kv_append != 0;
+    g.n_events = per * L + (tc ? 1 : 0);
     g.l2_prefetch_bytes = opt.l2_prefetch_kb * 1024;
     g.max_inflight = opt.max_inflight;
     if (g.tps < 1) return MK_ERR_INVALID;
@@ -208,15 +210,24 @@ mk_status build_plan(const mk_model_cfg &cfg, const mk_plan_options &opt, PlanTa
     uint32_t x_ready_cnt = 0;
     if (tc) {
         // embedding rows and the first RMSNorm statistics, one item per (sequence, H tile)
-        const uint16_t ev = (uint16_t)(5 * L);
+        const uint16_t ev = (uint16_t)(per * L);
         x_ready_cnt = emit_ranges(OP_EMBED, 0, B * g.h_tiles, kNoEvent, 0, ev);
         x_ready_ev = ev;
     }
     const uint32_t n_qkv = count_ranges(items(OP_QKV)), n_o = count_ranges(items(OP_O)),
                    n_gu = count_ranges(items(OP_GU)), n_down = count_ranges(items(OP_DOWN));
+    auto ev = [&](int32_t l, int32_t op) { return (uint16_t)ev_id(l, op, per); };
     for (int32_t l = 0; l < L; ++l) {
-        uint32_t k = emit_ranges(OP_QKV, l, items(OP_QKV), x_ready_ev, x_ready_cnt, (uint16_t)ev_id(l, OP_QKV));
+        uint32_t k = emit_ranges(OP_QKV, l, items(OP_QKV), x_ready_ev, x_ready_cnt, ev(l, OP_QKV));
         if (k != n_qkv) return MK_ERR_INVALID;
+        // attention waits for every row's q (and, in kv-append graphs, for
+        // every row's K/V in the cache: rows of one sequence attend to each other)
+        uint16_t att_ev = ev(l, OP_QKV);
+        uint32_t att_cnt = n_qkv;
+        if (opt.kv_append) {
+            att_cnt = emit_ranges(OP_KVA, l, B * nkv, ev(l, OP_QKV), n_qkv, ev(l, OP_KVA));
+            att_ev = ev(l, OP_KVA);
+        }
         // attention: one task per (sequence, kv head, split), round-robin over CTAs
         int32_t i = 0;
         for (int32_t b = 0; b < B; ++b)
@@ -225,19 +236,19 @@ mk_status build_plan(const mk_model_cfg &cfg, const mk_plan_options &opt, PlanTa
                     Task t{};
                     t.op = OP_ATTN;
                     t.layer = (uint16_t)l;
-                    t.wait_ev = (uint16_t)ev_id(l, OP_QKV);
-                    t.wait_count = n_qkv;
-                    t.signal_ev = (uint16_t)ev_id(l, OP_ATTN);
+                    t.wait_ev = att_ev;
+                    t.wait_count = att_cnt;
+                    t.signal_ev = ev(l, OP_ATTN);
                     t.a0 = b;
                     t.a1 = h;
                     t.a2 = s;
                     t.a3 = S;
                     q[perm[i % N]].push_back(t);
                 }
-        emit_ranges(OP_O, l, items(OP_O), (uint16_t)ev_id(l, OP_ATTN), (uint32_t)(B * nkv), (uint16_t)ev_id(l, OP_O));
-        emit_ranges(OP_GU, l, items(OP_GU), (uint16_t)ev_id(l, OP_O), n_o, (uint16_t)ev_id(l, OP_GU));
-        emit_ranges(OP_DOWN, l, items(OP_DOWN), (uint16_t)ev_id(l, OP_GU), n_gu, (uint16_t)ev_id(l, OP_DOWN));
-        x_ready_ev = (uint16_t)ev_id(l, OP_DOWN);
+        emit_ranges(OP_O, l, items(OP_O), ev(l, OP_ATTN), (uint32_t)(B * nkv), ev(l, OP_O));
+        emit_ranges(OP_GU, l, items(OP_GU), ev(l, OP_O), n_o, ev(l, OP_GU));
+        emit_ranges(OP_DOWN, l, items(OP_DOWN), ev(l, OP_GU), n_gu, ev(l, OP_DOWN));
+        x_ready_ev = ev(l, OP_DOWN);
         x_ready_cnt = n_down;
     }
     emit_ranges(OP_LM, L - 1, items(OP_LM), x_ready_ev, x_ready_cnt, kNoEvent);

@@ -17,6 +17,7 @@ struct PlanGeom {
     int32_t n_events = 0;
     int32_t l2_prefetch_bytes = 0;
     int32_t max_inflight = 0;  // ring copies in flight per CTA (0: no limit)
+    bool kv_append = false;    // K/V appended by OP_KVA tasks before attention
     MvGeom mv[OP_COUNT] = {};
     // batched (tensor-core) path
     bool tc = false;
@@ -43,10 +44,10 @@ mk_status check_cfg(const mk_model_cfg &cfg);
 // Builds the task graph for cfg on opt.num_ctas worker CTAs.
 mk_status build_plan(const mk_model_cfg &cfg, const mk_plan_options &opt, PlanTables *out);
 
-// Event ids.
-inline int32_t ev_id(int32_t layer, int32_t op) {
-    // per layer: QKV, ATTN, O, GU, DOWN
-    return layer * 5 + (op - 1);
+// Event ids: per layer QKV, ATTN, O, GU, DOWN, then KV-APPEND in graphs
+// that append K/V in a task of their own (per = 6; otherwise per = 5).
+inline int32_t ev_id(int32_t layer, int32_t op, int32_t per) {
+    return layer * per + (op == OP_KVA ? 5 : op - 1);
 }
 
 }  // namespace mk

@@ -12,7 +12,7 @@ from collections import defaultdict
 
 import numpy as np
 
-OP_NAMES = {1: "qkv", 2: "attn", 3: "o", 4: "gate_up", 5: "down", 6: "lm_head"}
+OP_NAMES = {1: "qkv", 2: "attn", 3: "o", 4: "gate_up", 5: "down", 6: "lm_head", 7: "embed", 8: "kv_append"}
 
 
 def _by_cta(tasks):

@@ -227,3 +227,29 @@ def test_attention_splits_cover_cached_blocks_once(S, pos):
     assert seen == list(range(nb))
     covered = {t for b in seen for t in range(64 * b, 64 * b + 64) if t < pos}
     assert covered == set(range(pos))
+
+
+@pytest.mark.parametrize("batch", [1, 64])
+def test_kv_append_graph_orders_append_between_qkv_and_attention(batch):
+    """The kv-append graph (the chunked-prefill engine's): per layer one
+    append item per (row, kv head), after every QKV task and before every
+    attention task, with the schedule still draining."""
+    m = SHAPES["8b"]
+    cfg = mk.model_cfg(m, batch, 1024)
+    tasks, n_events = mk.mk_plan_describe(cfg, 148, mk.mk_plan_options(kv_append=1, tensor_cores=1))
+    kva = [t for t in tasks if t.op == mk.OP_KVA]
+    for l in range(m.n_layers):
+        items = sorted((t.a0, t.a1) for t in kva if t.layer == l)
+        assert items[0][0] == 0 and items[-1][1] == batch * m.n_kv_heads
+        assert all(a[1] == b[0] for a, b in zip(items, items[1:]))
+    ok, order, _ = simulate(m, tasks, n_events)
+    assert ok, "deadlock"
+    pos = defaultdict(list)
+    for i, t in enumerate(order):
+        pos[(t.layer, t.op)].append(i)
+    for l in range(m.n_layers):
+        assert min(pos[(l, mk.OP_KVA)]) > max(pos[(l, mk.OP_QKV)])
+        assert min(pos[(l, mk.OP_ATTN)]) > max(pos[(l, mk.OP_KVA)])
+    att = [t for t in tasks if t.op == mk.OP_ATTN]
+    kva_ev = {t.signal_event for t in kva}
+    assert all(t.wait_event in kva_ev for t in att)
