@@ -194,6 +194,18 @@ mk_status mk_decode_step_host(mk_plan *plan, const int32_t *tokens_host, const i
 mk_status mk_prefill(mk_plan *plan, const int32_t *tokens, int32_t T, const mk_kv_cache *kv, float *last_logits,
                      void *stream);
 
+/* Passage: the throughput regime of "Llama-70B 向け…megakernel", section
+ * 高スループットMegakernelの設計と工夫 (large batches of sequences that arrive
+ * and leave), on one GPU.
+ * Prefill the T prompt tokens (device int32 [T]) of ONE batch row at
+ * positions 0..T-1, into the pages its page-table row names, with the
+ * chunked-prefill engine (made on first use, allocating device memory),
+ * whatever the plan's batch; the other rows' cache entries are untouched.
+ * Writes the logits of position T-1 (device fp32 [vocab]).  Continuous
+ * batching admits a sequence into a free row with this call. */
+mk_status mk_prefill_row(mk_plan *plan, int32_t row, const int32_t *tokens, int32_t T, const mk_kv_cache *kv,
+                         float *logits, void *stream);
+
 /* Passage: greedy decoding of the measured runs ("Valor central de MPK").
  * Greedy continuation for the next step: tokens[b] = argmax_v logits[b][v]
  * (lowest index on ties) and positions[b] += 1, on the device. */
@@ -266,6 +278,45 @@ mk_status mk_plan_trace(mk_plan *plan, void *stream, uint64_t *out, int64_t capa
  * mk_plan_create and mk_decode_step. */
 mk_status mk_decode_step_noalloc(const mk_model_cfg *cfg, const mk_weight_ptrs *w, const int32_t *tokens,
                                  const int32_t *positions, const mk_kv_cache *kv, float *logits, void *stream);
+
+/* ---------------------------------------------------------------------
+ * Continuous batching: a host-side allocator of the KV pool's pages and of
+ * the batch's page table (no GPU needed except for mk_pages_sync).
+ * Passage: the serving regime of "Llama-70B 向け…megakernel", section
+ * 高スループットMegakernelの設計と工夫 (sequences of different lengths
+ * sharing large decode batches), on one GPU.
+ *
+ * A plan's batch is a fixed set of rows.  Between decode steps a sequence is
+ * admitted into a free row (pages for its prompt), grows page by page as it
+ * decodes (mk_pages_extend before the step that writes a position its
+ * pages do not cover) and retires, its pages going back to the pool.  The
+ * pool's last page is scratch: every entry of a free row names it, so a
+ * decode step over the whole batch may run a free row (token 0, position 0)
+ * without touching any sequence's pages.  Errors: MK_ERR_INVALID for a bad
+ * row or state (admitting a live row, extending or retiring a free one, a
+ * length past max_pages_per_seq pages), MK_ERR_OOM when the pool has too
+ * few free pages (nothing is allocated then).
+ * --------------------------------------------------------------------- */
+typedef struct mk_page_pool mk_page_pool; /* opaque, host-side */
+
+/* num_pages: pages of the KV pools (the last one becomes scratch). */
+mk_status mk_pages_create(int32_t num_pages, int32_t batch, int32_t max_pages_per_seq, int32_t page_size,
+                          mk_page_pool **out);
+/* Row becomes live with pages for its first n_tokens positions. */
+mk_status mk_pages_admit(mk_page_pool *pool, int32_t row, int32_t n_tokens);
+/* A live row's pages cover its first n_tokens positions (no-op if they do). */
+mk_status mk_pages_extend(mk_page_pool *pool, int32_t row, int32_t n_tokens);
+/* A live row's pages return to the pool; its entries name the scratch page. */
+mk_status mk_pages_retire(mk_page_pool *pool, int32_t row);
+int32_t mk_pages_free_count(const mk_page_pool *pool);
+int32_t mk_pages_scratch_page(const mk_page_pool *pool);
+/* Host copy of the page table, int32 [batch][max_pages_per_seq]. */
+mk_status mk_pages_table(const mk_page_pool *pool, int32_t *out, int64_t capacity);
+/* Copies the page table (if it changed since the last sync) to the device
+ * table (int32 [batch][max_pages_per_seq]) on `stream`; the host copy may
+ * change again as soon as the call returns. */
+mk_status mk_pages_sync(mk_page_pool *pool, int32_t *page_table_dev, void *stream);
+void mk_pages_destroy(mk_page_pool *pool);
 
 /* Passage: none on the pages (error reporting of this library).
  * Synchronises `stream`, reads and clears the plan's device error word, and

@@ -57,9 +57,11 @@ class mk_task_info(ctypes.Structure):
 
 _lib = None
 EXPORTS = ("mk_plan_create", "mk_plan_create_ex", "mk_decode_step", "mk_decode_step_ablation",
-           "mk_decode_step_host", "mk_prefill", "mk_greedy_next", "mk_plan_last_error", "mk_status_string",
-           "mk_error_site_string", "mk_plan_destroy", "mk_plan_describe", "mk_plan_trace", "mk_decode_step_noalloc",
-           "mk_decode_step_greedy")
+           "mk_decode_step_host", "mk_prefill", "mk_prefill_row", "mk_greedy_next", "mk_plan_last_error",
+           "mk_status_string", "mk_error_site_string", "mk_plan_destroy", "mk_plan_describe", "mk_plan_trace",
+           "mk_decode_step_noalloc", "mk_decode_step_greedy", "mk_pages_create", "mk_pages_admit",
+           "mk_pages_extend", "mk_pages_retire", "mk_pages_free_count", "mk_pages_scratch_page", "mk_pages_table",
+           "mk_pages_sync", "mk_pages_destroy")
 
 
 def lib():
@@ -89,8 +91,19 @@ def lib():
                                        P(_i32), P(_i32)]
         L.mk_plan_trace.argtypes = [_vp, _vp, _vp, ctypes.c_int64, P(_i32), P(_i32)]
         L.mk_decode_step_noalloc.argtypes = [P(mk_model_cfg), P(mk_weight_ptrs), _vp, _vp, P(mk_kv_cache), _vp, _vp]
+        L.mk_prefill_row.argtypes = [_vp, _i32, _vp, _i32, P(mk_kv_cache), _vp, _vp]
+        L.mk_pages_create.argtypes = [_i32, _i32, _i32, _i32, P(_vp)]
+        L.mk_pages_admit.argtypes = [_vp, _i32, _i32]
+        L.mk_pages_extend.argtypes = [_vp, _i32, _i32]
+        L.mk_pages_retire.argtypes = [_vp, _i32]
+        L.mk_pages_free_count.argtypes = [_vp]
+        L.mk_pages_scratch_page.argtypes = [_vp]
+        L.mk_pages_table.argtypes = [_vp, _vp, ctypes.c_int64]
+        L.mk_pages_sync.argtypes = [_vp, _vp, _vp]
+        L.mk_pages_destroy.argtypes = [_vp]
+        L.mk_pages_destroy.restype = None
         for n in EXPORTS:
-            if n not in ("mk_plan_destroy", "mk_status_string", "mk_error_site_string"):
+            if n not in ("mk_plan_destroy", "mk_status_string", "mk_error_site_string", "mk_pages_destroy"):
                 getattr(L, n).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -164,6 +177,56 @@ class KVCache:
                                 self.max_pages)
 
 
+class PagePool:
+    """Host-side allocator of a KV pool's pages and of the batch's page table
+    (mk_pages_* in include/mk.h): rows are admitted, extended and retired
+    between decode steps; sync() copies the table to the device."""
+
+    def __init__(self, num_pages: int, batch: int, max_pages: int, page_size: int = 64):
+        self.batch, self.max_pages = batch, max_pages
+        h = _vp()
+        _check(lib().mk_pages_create(num_pages, batch, max_pages, page_size, ctypes.byref(h)), "mk_pages_create")
+        self.h = h
+
+    def admit(self, row: int, n_tokens: int) -> int:
+        return lib().mk_pages_admit(self.h, row, n_tokens)
+
+    def extend(self, row: int, n_tokens: int) -> int:
+        return lib().mk_pages_extend(self.h, row, n_tokens)
+
+    def retire(self, row: int) -> int:
+        return lib().mk_pages_retire(self.h, row)
+
+    @property
+    def free_count(self) -> int:
+        return int(lib().mk_pages_free_count(self.h))
+
+    @property
+    def scratch_page(self) -> int:
+        return int(lib().mk_pages_scratch_page(self.h))
+
+    def table(self):
+        import numpy as np
+
+        out = np.empty((self.batch, self.max_pages), dtype=np.int32)
+        _check(lib().mk_pages_table(self.h, out.ctypes.data, out.size), "mk_pages_table")
+        return out
+
+    def sync(self, page_table_dev, stream=None) -> None:
+        _check(lib().mk_pages_sync(self.h, page_table_dev.data_ptr(), _stream_ptr(stream)), "mk_pages_sync")
+
+    def close(self):
+        if self.h:
+            lib().mk_pages_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 class Plan:
     """Owns an mk_plan plus references to the weight tensors it points at."""
 
@@ -224,6 +287,12 @@ class Plan:
         T = tokens.shape[-1]
         _check(lib().mk_prefill(self.h, tokens.data_ptr(), T, ctypes.byref(kv.desc), last_logits.data_ptr(),
                                 _stream_ptr(stream)), "mk_prefill")
+
+    def prefill_row(self, row: int, tokens, kv: KVCache, logits, stream=None):
+        """Prefill one batch row's prompt (device int32 [T]) into its pages; logits: device fp32 [vocab]."""
+        T = tokens.shape[-1]
+        _check(lib().mk_prefill_row(self.h, row, tokens.data_ptr(), T, ctypes.byref(kv.desc), logits.data_ptr(),
+                                    _stream_ptr(stream)), "mk_prefill_row")
 
     def greedy_next(self, logits, tokens, positions, stream=None):
         _check(lib().mk_greedy_next(self.h, logits.data_ptr(), tokens.data_ptr(), positions.data_ptr(),

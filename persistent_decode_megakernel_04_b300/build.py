@@ -13,7 +13,7 @@ LIB = PKG / "libmk.so"
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
                      "-I", str(ROOT / "include")]
-UNITS = ["megakernel.cu", "api.cu", "planner.cpp", "noalloc.cu"]
+UNITS = ["megakernel.cu", "api.cu", "planner.cpp", "noalloc.cu", "pages.cpp"]
 
 
 def _sources():

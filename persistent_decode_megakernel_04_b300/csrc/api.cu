@@ -629,34 +629,30 @@ mk_status ensure_prefill_engine(mk_plan *p) {
     return MK_OK;
 }
 
-// Prefill of every sequence's T tokens through the engine: chunks of up to
-// kPrefillRows consecutive tokens, one launch each (the rows past a short
-// last chunk repeat its last token at its position: they write the same K/V
-// to the same slot and are not read); the LM head runs on the last chunk only.
-mk_status prefill_chunked(mk_plan *p, const int32_t *tokens, int32_t T, const mk_kv_cache *kv, float *last_logits,
-                          cudaStream_t s) {
+// Prefill of the T tokens of batch row `row` (its page-table row) through
+// the engine: chunks of up to kPrefillRows consecutive tokens, one launch
+// each (the rows past a short last chunk repeat its last token at its
+// position: they write the same K/V to the same slot and are not read); the
+// LM head runs on the last chunk only, whose last row's logits go to `logits`.
+mk_status prefill_seq(mk_plan *p, int32_t row, const int32_t *tokens, int32_t T, const mk_kv_cache *kv,
+                      float *logits, cudaStream_t s) {
     mk_plan *q = p->pre;
     mk_status st = check_kv(q, kv);
     if (st != MK_OK) return st;
     const int32_t V = p->cfg.vocab;
-    for (int32_t b = 0; b < p->cfg.batch; ++b) {
-        int32_t n = 0;
-        for (int32_t c0 = 0; c0 < T; c0 += kPrefillRows) {
-            n = std::min(kPrefillRows, T - c0);
-            cudaError_t e = launch_prefill_rows(tokens + (int64_t)b * T + c0, n, c0, kPrefillRows, p->d_pre_tok,
-                                                p->d_pre_pos, s);
-            if (e != cudaSuccess) return cuda_status(e);
-            KParams k = step_params(q, p->d_pre_tok, 1, p->d_pre_pos, 1, kv, p->d_pre_logits);
-            k.page_table = kv->page_table + (int64_t)b * kv->max_pages_per_seq;
-            k.pt_stride = 0;  // every row is a token of sequence b
-            k.skip_lm = (c0 + n < T) ? 1 : 0;
-            if ((st = launch_step(q, k, s)) != MK_OK) return st;
-        }
-        const cudaError_t e = cudaMemcpyAsync(last_logits + (int64_t)b * V, p->d_pre_logits + (int64_t)(n - 1) * V,
-                                              (size_t)V * sizeof(float), cudaMemcpyDeviceToDevice, s);
+    int32_t n = 0;
+    for (int32_t c0 = 0; c0 < T; c0 += kPrefillRows) {
+        n = std::min(kPrefillRows, T - c0);
+        const cudaError_t e = launch_prefill_rows(tokens + c0, n, c0, kPrefillRows, p->d_pre_tok, p->d_pre_pos, s);
         if (e != cudaSuccess) return cuda_status(e);
+        KParams k = step_params(q, p->d_pre_tok, 1, p->d_pre_pos, 1, kv, p->d_pre_logits);
+        k.page_table = kv->page_table + (int64_t)row * kv->max_pages_per_seq;
+        k.pt_stride = 0;  // every row of the launch is a token of this sequence
+        k.skip_lm = (c0 + n < T) ? 1 : 0;
+        if ((st = launch_step(q, k, s)) != MK_OK) return st;
     }
-    return MK_OK;
+    return cuda_status(cudaMemcpyAsync(logits, p->d_pre_logits + (int64_t)(n - 1) * V, (size_t)V * sizeof(float),
+                                       cudaMemcpyDeviceToDevice, s));
 }
 
 }  // namespace
@@ -672,14 +668,29 @@ mk_status mk_prefill(mk_plan *p, const int32_t *tokens, int32_t T, const mk_kv_c
     // chunked prefill when a launch of kPrefillRows tokens of one sequence
     // beats a launch of one token of each sequence
     if (T > 1 && p->cfg.batch < kPrefillRows && p->opt.prefill_by_decode == 0 &&
-        ensure_prefill_engine(p) == MK_OK)
-        return prefill_chunked(p, tokens, T, kv, last_logits, s);
+        ensure_prefill_engine(p) == MK_OK) {
+        for (int32_t b = 0; b < p->cfg.batch; ++b)
+            if ((st = prefill_seq(p, b, tokens + (int64_t)b * T, T, kv, last_logits + (int64_t)b * p->cfg.vocab, s)) !=
+                MK_OK)
+                return st;
+        return MK_OK;
+    }
     for (int32_t t = 0; t < T; ++t) {
         KParams k = step_params(p, tokens + t, T, p->d_iota + t, 0, kv, last_logits);
         k.skip_lm = (t + 1 < T) ? 1 : 0;
         if ((st = launch_step(p, k, s)) != MK_OK) return st;
     }
     return MK_OK;
+}
+
+mk_status mk_prefill_row(mk_plan *p, int32_t row, const int32_t *tokens, int32_t T, const mk_kv_cache *kv,
+                         float *logits, void *stream) {
+    if (!p || !tokens || !logits || row < 0 || row >= p->cfg.batch || T <= 0 || T > p->cfg.max_seq)
+        return MK_ERR_INVALID;
+    mk_status st = check_kv(p, kv);
+    if (st != MK_OK) return st;
+    if ((st = ensure_prefill_engine(p)) != MK_OK) return st;
+    return prefill_seq(p, row, tokens, T, kv, logits, static_cast<cudaStream_t>(stream));
 }
 
 mk_status mk_greedy_next(mk_plan *p, const float *logits, int32_t *tokens, int32_t *positions, void *stream) {

@@ -157,3 +157,71 @@ def test_70b_batched_first_decode_step(cuda_device):
             model.layer_step(lw, kc, vc, ctx, xs[b])
     for b in rows:
         harness.compare_logits(got[b], model.head(xs[b]), f"70B row {b}")
+
+
+def test_continuous_batching_admits_grows_and_retires_sequences(cuda_device):
+    """Continuous batching on a 4-row plan over a 10-page pool: sequences are
+    admitted into free rows (prompt prefilled into the row's own pages by
+    mk_prefill_row), decode with their own positions, grow page by page
+    (one crosses a page boundary mid-run), retire, and a later sequence
+    reuses the freed pages; a row never admitted runs on the scratch page.
+    Every live row's logits match the oracle at every step (teacher
+    forcing: each is fed the oracle's greedy token)."""
+    import torch
+
+    m = TINY
+    B, max_seq, page = 4, 256, 64
+    plan, _ = harness.gpu_plan(m, max_seq, batch=B)
+    kv = mk.KVCache(m, B, max_seq, num_pages=10)
+    pool = mk.PagePool(10, B, kv.max_pages, page)
+    model = harness.oracle_model(m)
+    live = {}  # row -> [oracle k cache, v cache, position, next token]
+    V = m.vocab
+
+    def admit(row, T, seq):
+        prompt = synth.tokens(T, 0, 300 + seq, V)
+        assert pool.admit(row, T) == mk.MK_OK
+        pool.sync(kv.page_table)
+        kc, vc = model.new_cache(max_seq)
+        ref = model.prefill(kc, vc, prompt)
+        out = torch.empty(V, dtype=torch.float32, device=cuda_device)
+        plan.prefill_row(row, torch.tensor(prompt, dtype=torch.int32, device=cuda_device), kv, out)
+        plan.check()
+        harness.compare_logits(out.cpu().numpy(), ref, f"prefill of row {row}")
+        live[row] = [kc, vc, T, int(np.argmax(ref))]
+
+    def step(i):
+        for row, st in live.items():
+            assert pool.extend(row, st[2] + 1) == mk.MK_OK
+        pool.sync(kv.page_table)
+        tok = np.zeros(B, np.int32)
+        pos = np.zeros(B, np.int32)
+        refs = {}
+        for row, st in live.items():
+            tok[row], pos[row] = st[3], st[2]
+            refs[row] = model.decode_step(st[0], st[1], st[3], st[2])
+        logits = torch.empty((B, V), dtype=torch.float32, device=cuda_device)
+        plan.decode_step(torch.tensor(tok, device=cuda_device), torch.tensor(pos, device=cuda_device), kv, logits)
+        plan.check()
+        got = logits.cpu().numpy()
+        for row, ref in refs.items():
+            harness.compare_logits(got[row], ref, f"step {i} row {row} (pos {pos[row]})")
+            live[row][2] += 1
+            live[row][3] = int(np.argmax(ref))
+
+    admit(0, 20, 0)
+    admit(2, 125, 1)  # crosses its second page boundary at position 128
+    for i in range(6):
+        step(i)
+    assert live[2][2] == 131 and pool.table()[2, 2] != pool.scratch_page
+    free_before = pool.free_count
+    assert pool.retire(0) == mk.MK_OK and pool.free_count == free_before + 1
+    del live[0]
+    admit(0, 33, 2)  # reuses the retired sequence's page
+    for i in range(6, 9):
+        step(i)
+    admit(3, 5, 3)
+    for i in range(9, 12):
+        step(i)
+    assert np.all(pool.table()[1] == pool.scratch_page)  # row 1 never admitted
+    pool.close()
