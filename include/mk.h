@@ -123,7 +123,13 @@ typedef struct {
                               last attention split appends its row's K/V itself */
     int32_t prefill_by_decode; /* 1: mk_prefill runs the decode step once per position instead of
                                   the chunked-prefill engine */
-    int32_t reserved[3];
+    int32_t jit;           /* 0: static dispatch, every task bound to a CTA ahead of time (default);
+                              n >= 1: dynamic dispatch: each CTA's scheduler warp claims the next
+                              unclaimed task of the earliest unfinished stage (a layer's operator)
+                              at run time, batch-1 projections cut into n ranges per CTA (at most
+                              16; the tensor-core path keeps one range per CTA).  Not with trace;
+                              the ablation build needs static dispatch */
+    int32_t reserved[2];
 } mk_plan_options;
 
 typedef struct mk_plan mk_plan; /* opaque, library-owned */

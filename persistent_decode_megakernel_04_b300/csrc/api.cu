@@ -51,6 +51,7 @@ struct mk_plan {
     // chunked-prefill engine, made on first use: a kv-append plan whose
     // kPrefillRows batch rows are consecutive tokens of one sequence
     mk_plan *pre = nullptr;
+    int32_t *d_stage_off = nullptr;  // dynamic dispatch: first task of each stage
     float *d_pre_logits = nullptr;  // [kPrefillRows][vocab]
     int32_t *d_pre_tok = nullptr, *d_pre_pos = nullptr;
     // tensor maps of the last KV cache seen (encoded once per cache, not per step)
@@ -263,10 +264,11 @@ mk_status mk_plan_describe(const mk_model_cfg *cfg, const mk_plan_options *opt, 
     *n_events = t.g.n_events;
     if (capacity < *n_tasks || (!out && *n_tasks > 0)) return MK_ERR_INVALID;
     for (int32_t c = 0; c < o.num_ctas; ++c)
-        for (int32_t i = t.queue_off[c]; i < t.queue_off[c + 1]; ++i) {
+        for (int32_t i = (t.g.jit ? (c == 0 ? 0 : *n_tasks) : t.queue_off[c]);
+             i < (t.g.jit ? (c == 0 ? *n_tasks : 0) : t.queue_off[c + 1]); ++i) {
             const Task &k = t.tasks[i];
             mk_task_info &d = out[i];
-            d.cta = c;
+            d.cta = t.g.jit ? -1 : c;  // dynamic dispatch: claimed at run time, stage by stage
             d.op = k.op;
             d.layer = k.layer;
             d.wait_event = k.wait_ev == kNoEvent ? -1 : k.wait_ev;
@@ -324,7 +326,7 @@ mk_status mk_plan_create_ex(const mk_model_cfg *cfg, const mk_weight_ptrs *w, co
         return MK_ERR_INVALID;
     }
     const int32_t max_k = std::max({cfg->hidden, cfg->ffn_dim, cfg->n_q_heads * cfg->head_dim});
-    p->variant = megakernel_variant(max_k, g.tc);
+    p->variant = megakernel_variant(max_k, g.tc, g.jit);
     if (megakernel_set_smem(p->variant, p->smem) != cudaSuccess) {
         cudaGetLastError();
         free_plan(p);
@@ -340,7 +342,8 @@ mk_status mk_plan_create_ex(const mk_model_cfg *cfg, const mk_weight_ptrs *w, co
     const mk_model_cfg &c = *cfg;
     const int32_t G = c.n_q_heads / c.n_kv_heads, S = g.attn_splits;
     const int32_t qkv_rows = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
-    p->cl = ctl_layout(g.n_events, c.batch * c.n_kv_heads, g.tc ? g.n_tile_ctrs : 0, c.batch);
+    const int32_t n_stages = g.jit ? (int32_t)p->tables.stage_off.size() - 1 : 0;
+    p->cl = ctl_layout(g.n_events, c.batch * c.n_kv_heads, g.tc ? g.n_tile_ctrs : 0, c.batch, n_stages);
     const size_t n_part = (size_t)c.batch * c.n_kv_heads * S * G * (c.head_dim + 2);
     if ((st = dev_alloc(p, &p->d_layers, c.n_layers)) || (st = dev_alloc(p, &p->d_tasks, p->tables.tasks.size())) ||
         (st = dev_alloc(p, &p->d_queue, p->tables.queue_off.size())) ||
@@ -354,6 +357,18 @@ mk_status mk_plan_create_ex(const mk_model_cfg *cfg, const mk_weight_ptrs *w, co
         (st = dev_alloc(p, &p->d_stage_logits, (size_t)c.batch * c.vocab))) {
         free_plan(p);
         return st;
+    }
+    if (g.jit) {
+        if ((st = dev_alloc(p, &p->d_stage_off, p->tables.stage_off.size())) != MK_OK) {
+            free_plan(p);
+            return st;
+        }
+        if (cudaMemcpy(p->d_stage_off, p->tables.stage_off.data(), p->tables.stage_off.size() * sizeof(int32_t),
+                       cudaMemcpyHostToDevice) != cudaSuccess) {
+            cudaGetLastError();
+            free_plan(p);
+            return MK_ERR_CUDA;
+        }
     }
     if (cudaHostAlloc(reinterpret_cast<void **>(&p->h_err), 4 * sizeof(uint32_t), cudaHostAllocDefault) !=
         cudaSuccess) {
@@ -504,6 +519,9 @@ mk_status mk_plan_create_ex(const mk_model_cfg *cfg, const mk_weight_ptrs *w, co
     k.only_layer = -1;
     k.skip_lm = 0;
     k.kv_appended = g.kv_append ? 1 : 0;
+    k.jit = g.jit ? 1 : 0;
+    k.n_stages = n_stages;
+    k.stage_off = p->d_stage_off;
     k.timeout_ns = (uint64_t)p->opt.timeout_ms * 1000000ull;
     k.trace = p->d_trace;
     k.trace_stride = p->trace_stride;
@@ -560,6 +578,7 @@ mk_status mk_decode_step_greedy(mk_plan *p, int32_t *tokens, int32_t *positions,
 mk_status mk_decode_step_ablation(mk_plan *p, const int32_t *tokens, const int32_t *positions,
                                   const mk_kv_cache *kv, float *logits, void *stream) {
     if (!p || !tokens || !positions || !logits) return MK_ERR_INVALID;
+    if (p->tables.g.jit) return MK_ERR_UNSUPPORTED;  // one operator per launch needs the static queues
     mk_status st = check_kv(p, kv);
     if (st != MK_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -68,6 +68,13 @@ struct SmemCtl {
     uint32_t abort;      // local abort flag
     uint32_t last_flag;  // attention: this CTA finished the last split of a head
     uint32_t pad0;
+    // dynamic dispatch: the tasks this CTA's scheduler claimed, a ring of
+    // task indices (the i-th claimed task in slot i % kJitRing)
+    uint32_t jq[kJitRing];
+    uint32_t jclaimed;   // tasks claimed so far
+    uint32_t jdone;      // 1 once every stage is exhausted (jclaimed is final)
+    uint32_t jprod;      // claimed tasks the producer has read
+    uint32_t jcomp;      // claimed tasks the compute warps have read
     float rms_part[kComputeWarps];
     unsigned long long amax_part[kComputeWarps];  // fused greedy pick: each warp's packed maximum
     float att_m[kMaxGroup], att_l[kMaxGroup], att_alpha[kMaxGroup];
@@ -204,7 +211,7 @@ __device__ __forceinline__ bool task_active(const KParams &p, const Task &t) {
 }
 
 __device__ __forceinline__ uint64_t *trace_slot(const KParams &p, int task) {
-    return p.trace ? p.trace + ((size_t)blockIdx.x * p.trace_stride + task) * 8 : nullptr;
+    return (p.trace && !p.jit) ? p.trace + ((size_t)blockIdx.x * p.trace_stride + task) * 8 : nullptr;
 }
 
 __device__ __forceinline__ bool global_abort(const KParams &p) {
@@ -254,6 +261,29 @@ __device__ bool wait_mbar(const Ctx &c, uint64_t *bar, uint32_t parity, int32_t 
             next = now + kAbortCheckNs;
         }
     }
+}
+
+// Dynamic dispatch: the i-th task this CTA's scheduler claimed.  Waits
+// (bounded) until it is claimed; false once every stage is exhausted and i
+// is past the last claim, or on abort or timeout (the CTA is then aborted).
+// The reader publishes i + 1 in *seen once it holds the task, so the
+// scheduler may reuse the ring slot.
+__device__ __noinline__ bool jit_task(const Ctx &c, int i, Task *t, uint32_t *seen) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if ((uint32_t)i < ld_acquire_cta(&c.sc->jclaimed)) break;
+        if (ld_acquire_cta(&c.sc->jdone) && (uint32_t)i >= ld_acquire_cta(&c.sc->jclaimed)) return false;
+        if ((it & 63u) == 0) {
+            if (local_abort(c)) return false;
+            if (globaltimer_ns() - t0 > 4 * c.p->timeout_ns) {
+                record_error(c, 4 /*MK_ERR_TIMEOUT*/, SITE_READY_WAIT, i);
+                return false;
+            }
+        }
+    }
+    *t = c.p->tasks[c.sc->jq[i % kJitRing]];
+    if (seen) st_release_cta(seen, (uint32_t)(i + 1));
+    return true;
 }
 
 // ----------------------------------------------------------------- pages
@@ -609,6 +639,7 @@ struct Producer {
     }
 };
 
+template <bool JIT>
 __device__ void producer_role(const Ctx &c, const Task *q, int nt) {
     if ((threadIdx.x & 31) != 0) return;
     Producer pr;
@@ -616,12 +647,18 @@ __device__ void producer_role(const Ctx &c, const Task *q, int nt) {
     pr.ns = (uint32_t)c.p->num_slots;
     pr.slot_bytes = (uint32_t)c.p->slot_bytes;
     pr.fmax = (c.p->max_inflight > 0 && (uint32_t)c.p->max_inflight < pr.ns) ? (uint32_t)c.p->max_inflight : 0u;
-    for (int i = 0; i < nt; ++i) {
-        const Task t = q[i];
+    for (int i = 0;; ++i) {
+        Task t;
+        if (JIT) {
+            if (!jit_task(c, i, &t, &c.sc->jprod)) break;
+        } else {
+            if (i >= nt) break;
+            t = q[i];
+        }
         if (!task_active(*c.p, t)) continue;
         pr.tr = trace_slot(*c.p, i);
         bool ok = true;
-        if (t.op == OP_O && !c.p->tc && c.p->l2_prefetch_bytes > 0)
+        if (t.op == OP_O && !c.p->tc && c.p->l2_prefetch_bytes > 0 && !JIT)
             pr.prefetch_past_attention(c, t, i + 1 < nt ? &q[i + 1] : nullptr);
         if (t.op == OP_ATTN) ok = (!c.p->kv_appended || pr.wait_released(c, i)) && pr.run_attn(c, t);
         else if (t.op == OP_EMBED || t.op == OP_KVA) ok = true;
@@ -712,11 +749,113 @@ __device__ void scheduler_loop(const Ctx &c, const Task *q, int nt, ActProducer 
     }
 }
 
+// Dynamic dispatch.  The scheduler claims tasks for its CTA at run time:
+// the next unclaimed task of the earliest stage with any left (one relaxed
+// atomicAdd on the stage's claim counter), as long as fewer than kJitRing
+// claimed tasks are ahead of the producer and the compute warps; then it
+// releases them in claim order once their events reach their thresholds,
+// claiming more while it waits (a ring slot is reused only once the
+// producer and the compute warps have read its task and the scheduler has
+// released it).  Every task of a stage is claimed before any
+// task of the next, and each CTA runs its claims in order, so a stage's
+// tasks never wait on a later stage's: the run cannot deadlock.
+__device__ __noinline__ void scheduler_loop_jit(const Ctx &c, ActProducer &ap) {
+    const KParams &p = *c.p;
+    SmemCtl *sc = c.sc;
+    uint32_t claimed = 0, released = 0;
+    int32_t stage = 0;
+    bool done = false;
+    auto try_claim = [&]() -> bool {
+        while (stage < p.n_stages) {
+            // a slot is free once the producer and the compute warps have
+            // read its task and this scheduler has released it
+            const uint32_t jcomp = ld_acquire_cta(&sc->jcomp);
+            const uint32_t behind = min(min(ld_acquire_cta(&sc->jprod), jcomp), released);
+            if (claimed - behind >= (uint32_t)kJitRing) return false;
+            // claim only kJitAhead tasks beyond the one the compute warps hold:
+            // a CTA that claimed far ahead would keep later stages' tasks from
+            // the idle CTAs, and one claim ahead lets the producer stream the
+            // next task's weights
+            if (claimed >= jcomp + (uint32_t)kJitAhead) return false;
+            const int32_t s0 = p.stage_off[stage], n = p.stage_off[stage + 1] - s0;
+            const uint32_t idx = atomicAdd(p.ctl + p.cl.claim_idx + stage, 1u);
+            if (idx < (uint32_t)n) {
+                sc->jq[claimed % kJitRing] = (uint32_t)(s0 + (int32_t)idx);
+                st_release_cta(&sc->jclaimed, ++claimed);
+                return true;
+            }
+            ++stage;
+        }
+        if (!done) {
+            st_release_cta(&sc->jdone, 1u);
+            done = true;
+        }
+        return false;
+    };
+    const uint64_t t_start = globaltimer_ns();
+    uint64_t next = t_start + kAbortCheckNs;
+    for (;;) {
+        while (try_claim()) {
+        }
+        if (released < claimed) {
+            const Task t = p.tasks[sc->jq[released % kJitRing]];
+            if (t.wait_ev != kNoEvent) {
+                const uint32_t *ctr = p.ctl + t.wait_ev;
+                const uint64_t t0 = globaltimer_ns();
+                uint64_t nx = t0 + kAbortCheckNs;
+                while (!(ld_relaxed_gpu(ctr) >= t.wait_count && ld_acquire_gpu(ctr) >= t.wait_count)) {
+                    try_claim();
+                    const uint64_t now = globaltimer_ns();
+                    if (now >= nx) {
+                        if (local_abort(c) || global_abort(p)) {
+                            set_local_abort(c);
+                            st_release_cta(&sc->ready, kReadyAbort);
+                            return;
+                        }
+                        if (now - t0 > p.timeout_ns) {
+                            record_error(c, 4, SITE_EVENT_WAIT, t.wait_ev);
+                            st_release_cta(&sc->ready, kReadyAbort);
+                            return;
+                        }
+                        nx = now + kAbortCheckNs;
+                    }
+                }
+            }
+            st_release_cta(&sc->ready, ++released);
+            if (p.tc && is_proj(t.op) && !ap.run(c, t)) {
+                st_release_cta(&sc->ready, kReadyAbort);
+                return;
+            }
+            next = globaltimer_ns() + kAbortCheckNs;
+        } else if (done) {
+            return;
+        } else {
+            // the ring is full of released tasks the compute warps have not taken yet
+            const uint64_t now = globaltimer_ns();
+            if (now >= next) {
+                if (local_abort(c) || global_abort(p)) {
+                    set_local_abort(c);
+                    st_release_cta(&sc->ready, kReadyAbort);
+                    return;
+                }
+                if (now - t_start > 4 * p.timeout_ns) {
+                    record_error(c, 4, SITE_EVENT_WAIT, -1);
+                    st_release_cta(&sc->ready, kReadyAbort);
+                    return;
+                }
+                next = now + kAbortCheckNs;
+            }
+        }
+    }
+}
+
+template <bool JIT>
 __device__ void scheduler_role(const Ctx &c, const Task *q, int nt) {
     if ((threadIdx.x & 31) != 0) return;
     ActProducer ap;
     ap.pol = policy_evict_last();
-    scheduler_loop(c, q, nt, ap);
+    if (JIT) scheduler_loop_jit(c, ap);
+    else scheduler_loop(c, q, nt, ap);
     if (c.p->tc) ap.drain(c);
 }
 
@@ -1973,7 +2112,7 @@ struct Consumer {
     }
 };
 
-template <int MAXCH>
+template <bool JIT>
 __device__ void compute_role(const Ctx &c, const Task *q, int nt) {
     const KParams &p = *c.p;
     Consumer cs;
@@ -1983,9 +2122,21 @@ __device__ void compute_role(const Ctx &c, const Task *q, int nt) {
     cs.ct = threadIdx.x - 64;
     cs.wc = cs.ct >> 5;
     cs.lane = threadIdx.x & 31;
-    cs.tracing = p.trace != nullptr && cs.ct == 0;
-    for (int i = 0; i < nt; ++i) {
-        const Task t = q[i];
+    cs.tracing = p.trace != nullptr && !JIT && cs.ct == 0;
+    for (int i = 0;; ++i) {
+        Task t;
+        if (JIT) {
+            // every compute thread reads the claimed task, then they meet (so
+            // that the slot is free again only once all hold it); the end of
+            // the claims is seen alike by all of them
+            const bool got = jit_task(c, i, &t, nullptr);
+            if (compute_bar_or(local_abort(c))) return;
+            if (!got) break;
+            if (cs.ct == 0) st_release_cta(&c.sc->jcomp, (uint32_t)(i + 1));
+        } else {
+            if (i >= nt) break;
+            t = q[i];
+        }
         if (!task_active(p, t)) continue;
         // wait for the scheduler to release task i
         if (ld_acquire_cta(&c.sc->ready) < (uint32_t)(i + 1)) {
@@ -2027,15 +2178,17 @@ __device__ void compute_role(const Ctx &c, const Task *q, int nt) {
     }
 }
 
-template <int MAXCH>
+// JIT: dynamic dispatch (tasks claimed at run time); otherwise every CTA
+// walks its static queue.
+template <bool JIT>
 __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant__ KParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     SmemCtl *sc = reinterpret_cast<SmemCtl *>(smem_raw);
     const uint32_t ctl_end = smem_u32(smem_raw) + (uint32_t)sizeof(SmemCtl);
     uint8_t *ring = smem_raw + (((ctl_end + 1023u) & ~1023u) - smem_u32(smem_raw));
     Ctx c{&p, sc, ring, ring + (size_t)p.num_slots * p.slot_bytes, (int)blockIdx.x};
-    const Task *q = p.tasks + p.queue_off[blockIdx.x];
-    const int nt = p.queue_off[blockIdx.x + 1] - p.queue_off[blockIdx.x];
+    const Task *q = JIT ? p.tasks : p.tasks + p.queue_off[blockIdx.x];
+    const int nt = JIT ? 0 : p.queue_off[blockIdx.x + 1] - p.queue_off[blockIdx.x];
     const int warp = threadIdx.x >> 5;
     constexpr int kWarpMma = 2;  // batched path: TMEM owner and MMA issuer (compute warp 0)
 
@@ -2058,6 +2211,7 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant_
         sc->ready = 0;
         sc->abort = global_abort(p) ? 1u : 0u;  // a recorded error stays sticky
         sc->last_flag = 0;
+        sc->jclaimed = sc->jdone = sc->jprod = sc->jcomp = 0;
         fence_mbar_init();
     }
     if (p.tc && warp == kWarpMma) {
@@ -2091,9 +2245,9 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant_
     }
     __syncthreads();
     if (!local_abort(c)) {
-        if (warp == kWarpSched) scheduler_role(c, q, nt);
-        else if (warp == kWarpProd) producer_role(c, q, nt);
-        else compute_role<MAXCH>(c, q, nt);
+        if (warp == kWarpSched) scheduler_role<JIT>(c, q, nt);
+        else if (warp == kWarpProd) producer_role<JIT>(c, q, nt);
+        else compute_role<JIT>(c, q, nt);
     }
     if (p.tc && threadIdx.x == kWarpMma * 32) {
         // no MMA may still be reading shared memory or writing TMEM at exit
@@ -2118,7 +2272,7 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant_
         uint32_t *ex = p.ctl + p.cl.exit_idx;
         const uint32_t old = atom_acq_rel_gpu_add(ex, 1u);
         if (old == gridDim.x - 1) {
-            for (int i = 0; i < p.cl.n_events + p.cl.n_done; ++i) p.ctl[i] = 0u;
+            for (int i = 0; i < p.cl.n_events + p.cl.n_done + p.cl.n_claims; ++i) p.ctl[i] = 0u;
             *ex = 0u;
             if (p.greedy && !p.skip_lm && (p.only_op < 0 || p.only_op == OP_LM) && !global_abort(p)) {
                 // fused greedy pick: every CTA's maximum is in
@@ -2195,12 +2349,12 @@ __global__ void prefill_rows_kernel(const int32_t *src, int32_t n, int32_t p0, i
     }
 }
 
-template <int MAXCH>
+template <bool JIT>
 const void *kernel_ptr() {
-    return reinterpret_cast<const void *>(&megakernel<MAXCH>);
+    return reinterpret_cast<const void *>(&megakernel<JIT>);
 }
 
-const void *variant_ptr(int /*variant*/) { return kernel_ptr<2>(); }
+const void *variant_ptr(int variant) { return variant == 1 ? kernel_ptr<true>() : kernel_ptr<false>(); }
 
 }  // namespace
 
@@ -2208,8 +2362,8 @@ size_t megakernel_smem_bytes(int32_t slot_bytes, int32_t num_slots, int32_t aslo
     return kRingOffset + (size_t)slot_bytes * num_slots + (size_t)aslot_bytes * num_aslots;
 }
 
-int megakernel_variant(int32_t /*max_k*/, bool /*tc*/) {
-    return 2;  // one build: matvec inputs past 4096 columns stream through L2
+int megakernel_variant(int32_t /*max_k*/, bool /*tc*/, bool jit) {
+    return jit ? 1 : 0;  // one build per dispatch mode; matvec inputs past 4096 columns stream through L2
 }
 
 cudaError_t megakernel_set_smem(int variant, size_t smem) {

@@ -26,6 +26,8 @@ constexpr int kMvResident = 2;    // matvec inputs of up to 2 x 2048 columns sta
 constexpr int kMvSuper = 2;       // longer inputs: row groups that stream piece by piece together, so that
                                   // each input piece is loaded once for all of them
 constexpr int kMaxASlots = 8;     // activation ring slots (batched path)
+constexpr int kJitRing = 8;       // dynamic dispatch: ring slots of claimed tasks
+constexpr int kJitAhead = 1;      // dynamic dispatch: claims beyond the task the compute warps hold
 
 struct KParams {
     // shape
@@ -55,6 +57,11 @@ struct KParams {
     // task graph
     const Task *tasks;
     const int32_t *queue_off;
+    // dynamic dispatch (0: static queues): stage s holds tasks
+    // [stage_off[s], stage_off[s + 1]); claim counters at ctl + cl.claim_idx
+    int32_t jit;
+    int32_t n_stages;
+    const int32_t *stage_off;
     MvGeom mv[OP_COUNT];
     int32_t slot_bytes, num_slots, attn_ts, attn_splits;  // attn_ts: KV tokens per ring slot
     int32_t l2_prefetch_bytes;
@@ -101,9 +108,8 @@ struct KParams {
 // ring of the batched path).
 size_t megakernel_smem_bytes(int32_t slot_bytes, int32_t num_slots, int32_t aslot_bytes, int32_t num_aslots);
 
-// Picks the register-tile variant for the longest matvec input (batch 1), or
-// the tensor-core variant (batched).
-int megakernel_variant(int32_t max_k, bool tc);
+// Picks the kernel build: static queues or dynamic dispatch.
+int megakernel_variant(int32_t max_k, bool tc, bool jit);
 
 // Launches the megakernel: cooperative (persistent mode) or plain (ablation).
 cudaError_t launch_megakernel(const KParams &p, int variant, int grid, size_t smem, bool cooperative,

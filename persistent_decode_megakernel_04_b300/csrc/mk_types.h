@@ -94,23 +94,27 @@ enum ErrSite : int32_t {
 // Layout of the plan's control words (uint32 each, zeroed at plan creation).
 //   [0, n_events)                           event counters
 //   [n_events, n_events + batch*n_kv_heads) attention split-done counters
-//   then n_tiles row-tile counters (batched path), then: exit counter, abort
+//   then n_claims claim counters (dynamic dispatch), n_tiles row-tile
+//   counters (batched path), then: exit counter, abort
 //   flag, error status, error site, error cta, error detail, then one 64-bit
 //   word per sequence (even index): the fused greedy pick's packed maximum
 struct CtlLayout {
     int32_t n_events;
     int32_t n_done;
+    int32_t claim_idx, n_claims;  // dynamic dispatch: one claim counter per stage
     int32_t tile_idx, n_tiles;
     int32_t exit_idx, abort_idx, err_idx;
     int32_t amax_idx;  // sequence b's packed (logit, index) maximum: words amax_idx + 2b, + 2b + 1
     int32_t total;
 };
 
-inline CtlLayout ctl_layout(int32_t n_events, int32_t n_done, int32_t n_tiles, int32_t n_seq) {
+inline CtlLayout ctl_layout(int32_t n_events, int32_t n_done, int32_t n_tiles, int32_t n_seq, int32_t n_claims = 0) {
     CtlLayout c;
     c.n_events = n_events;
     c.n_done = n_done;
-    c.tile_idx = n_events + n_done;
+    c.claim_idx = n_events + n_done;
+    c.n_claims = n_claims;
+    c.tile_idx = c.claim_idx + n_claims;
     c.n_tiles = n_tiles;
     c.exit_idx = c.tile_idx + n_tiles;
     c.abort_idx = c.exit_idx + 1;

@@ -167,7 +167,7 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_model_cfg *cfg, const mk_we
 
     const size_t smem = megakernel_smem_bytes(g.slot_bytes, g.num_slots, 0, 0);
     if ((int)smem > smem_optin) return MK_ERR_INVALID;
-    const int variant = megakernel_variant(std::max({c.hidden, c.ffn_dim, c.n_q_heads * c.head_dim}), false);
+    const int variant = megakernel_variant(std::max({c.hidden, c.ffn_dim, c.n_q_heads * c.head_dim}), false, false);
     int per_sm = 0;
     if (megakernel_set_smem(variant, smem) != cudaSuccess ||
         megakernel_max_active(variant, smem, &per_sm) != cudaSuccess) {

@@ -115,6 +115,7 @@ mk_status build_plan(const mk_model_cfg &cfg, const mk_plan_options &opt, PlanTa
     if (st != MK_OK) return st;
     const int32_t N = opt.num_ctas;
     const bool tc = cfg.batch > 1 || opt.tensor_cores == 1;
+    if (opt.jit < 0 || opt.jit > 16 || (opt.jit > 0 && opt.trace)) return MK_ERR_INVALID;
     if (N <= 0 || opt.slot_bytes < 4096 || opt.slot_bytes % 1024 || opt.attn_splits <= 0 ||
         opt.attn_splits > kMaxSplits || (tc ? (opt.num_slots == 1 || opt.num_slots < 0) : opt.num_slots < 2))
         return MK_ERR_INVALID;
@@ -182,13 +183,31 @@ mk_status build_plan(const mk_model_cfg &cfg, const mk_plan_options &opt, PlanTa
     auto items = [&](int32_t op) -> int32_t { return tc ? g.tcg[op].units : g.mv[op].rows; };
 
     std::vector<std::vector<Task>> q(N);
-    // Cuts `total` items into one contiguous range per CTA (balanced to one
-    // item); range c goes to CTA perm[c].  Returns the number of tasks.
+    // Dynamic dispatch (opt.jit): no task is bound to a CTA.  The tasks of
+    // each stage (a layer's operator) sit together in stage order, and at run
+    // time every CTA's scheduler claims the next unclaimed task of the
+    // earliest unfinished stage.  Batch-1 projections are cut into jit ranges
+    // per CTA, so that faster CTAs take more of them; the tensor-core path
+    // keeps one range per CTA (its row-tile fixups are numbered by range).
+    const bool jit = opt.jit > 0;
+    const int32_t R = (jit && !tc) ? opt.jit * N : N;  // ranges per projection stage
+    std::vector<Task> flat;
+    std::vector<int32_t> stage_off;
+    auto begin_stage = [&]() {
+        if (jit) stage_off.push_back((int32_t)flat.size());
+    };
+    auto push = [&](const Task &t, int32_t c) {
+        if (jit) flat.push_back(t);
+        else q[perm[c % N]].push_back(t);
+    };
+    // Cuts `total` items into R contiguous ranges (balanced to one item);
+    // static dispatch gives range c to CTA perm[c].  Returns the number of tasks.
     auto emit_ranges = [&](int32_t op, int32_t layer, int32_t total, uint16_t wait_ev, uint32_t wait_cnt,
                            uint16_t sig_ev) -> uint32_t {
         uint32_t n = 0;
-        for (int32_t c = 0; c < N; ++c) {
-            int32_t r0 = (int32_t)((int64_t)c * total / N), r1 = (int32_t)((int64_t)(c + 1) * total / N);
+        begin_stage();
+        for (int32_t c = 0; c < R; ++c) {
+            int32_t r0 = (int32_t)((int64_t)c * total / R), r1 = (int32_t)((int64_t)(c + 1) * total / R);
             if (r1 <= r0) continue;
             Task t{};
             t.op = (uint8_t)op;
@@ -199,12 +218,12 @@ mk_status build_plan(const mk_model_cfg &cfg, const mk_plan_options &opt, PlanTa
             t.a0 = r0;
             t.a1 = r1;
             t.a2 = c;
-            q[perm[c]].push_back(t);
+            push(t, c);
             ++n;
         }
         return n;
     };
-    auto count_ranges = [&](int32_t total) { return (uint32_t)std::min<int64_t>(total, N); };
+    auto count_ranges = [&](int32_t total) { return (uint32_t)std::min<int64_t>(total, R); };
 
     uint16_t x_ready_ev = kNoEvent;
     uint32_t x_ready_cnt = 0;
@@ -229,6 +248,7 @@ mk_status build_plan(const mk_model_cfg &cfg, const mk_plan_options &opt, PlanTa
             att_ev = ev(l, OP_KVA);
         }
         // attention: one task per (sequence, kv head, split), round-robin over CTAs
+        begin_stage();
         int32_t i = 0;
         for (int32_t b = 0; b < B; ++b)
             for (int32_t h = 0; h < nkv; ++h)
@@ -243,7 +263,7 @@ mk_status build_plan(const mk_model_cfg &cfg, const mk_plan_options &opt, PlanTa
                     t.a1 = h;
                     t.a2 = s;
                     t.a3 = S;
-                    q[perm[i % N]].push_back(t);
+                    push(t, i);
                 }
         emit_ranges(OP_O, l, items(OP_O), ev(l, OP_ATTN), (uint32_t)(B * nkv), ev(l, OP_O));
         emit_ranges(OP_GU, l, items(OP_GU), ev(l, OP_O), n_o, ev(l, OP_GU));
@@ -259,7 +279,18 @@ mk_status build_plan(const mk_model_cfg &cfg, const mk_plan_options &opt, PlanTa
         for (auto &qq : q)
             for (Task &t : qq)
                 if (t.wait_ev == ev) ++t.wait_count;
+        for (Task &t : flat)
+            if (t.wait_ev == ev) ++t.wait_count;
     }
+    g.jit = jit;
+    if (jit) {
+        out->tasks = flat;
+        stage_off.push_back((int32_t)flat.size());
+        out->stage_off = stage_off;
+        out->queue_off.assign(N + 1, 0);  // no task is bound to a CTA
+        return MK_OK;
+    }
+    out->stage_off.clear();
     out->tasks.clear();
     out->queue_off.assign(N + 1, 0);
     for (int32_t c = 0; c < N; ++c) {

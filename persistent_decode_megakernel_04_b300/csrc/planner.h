@@ -18,6 +18,7 @@ struct PlanGeom {
     int32_t l2_prefetch_bytes = 0;
     int32_t max_inflight = 0;  // ring copies in flight per CTA (0: no limit)
     bool kv_append = false;    // K/V appended by OP_KVA tasks before attention
+    bool jit = false;          // dynamic dispatch: CTAs claim tasks stage by stage at run time
     MvGeom mv[OP_COUNT] = {};
     // batched (tensor-core) path
     bool tc = false;
@@ -31,8 +32,9 @@ struct PlanGeom {
 
 struct PlanTables {
     PlanGeom g;
-    std::vector<Task> tasks;          // CTA 0's queue, then CTA 1's, ...
+    std::vector<Task> tasks;          // CTA 0's queue, then CTA 1's, ... (dynamic dispatch: stage by stage)
     std::vector<int32_t> queue_off;   // [num_ctas + 1]
+    std::vector<int32_t> stage_off;   // dynamic dispatch: first task of each stage, then the task count
 };
 
 // Fills in defaults for zero option fields.

@@ -225,3 +225,11 @@ def test_continuous_batching_admits_grows_and_retires_sequences(cuda_device):
         step(i)
     assert np.all(pool.table()[1] == pool.scratch_page)  # row 1 never admitted
     pool.close()
+
+
+def test_tiny_batched_dynamic_dispatch(cuda_device):
+    """Batched (tensor-core) plan under dynamic dispatch against the oracle."""
+    max_seq = 128
+    plan, kv = harness.gpu_plan(TINY, max_seq, batch=8, opts=mk.mk_plan_options(jit=1))
+    model = harness.oracle_model(TINY)
+    harness.run_teacher_forced_batch(plan, kv, model, prompts(8, 40, seed=6), 4, max_seq, rows=[0, 3, 7])

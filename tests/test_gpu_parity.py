@@ -406,3 +406,35 @@ def test_tiny_long_matvec_inputs(cuda_device, m, opts):
     plan, kv = harness.gpu_plan(m, 128, opts=mk.mk_plan_options(**opts) if opts else None)
     model = harness.oracle_model(m)
     harness.run_teacher_forced(plan, kv, model, synth.tokens(24, 0, 13, m.vocab), 4, 128)
+
+
+@pytest.mark.parametrize("opts", [dict(jit=1), dict(jit=4), dict(jit=2, num_ctas=7, attn_splits=3),
+                                  dict(jit=1, num_ctas=1, attn_splits=2)],
+                         ids=["jit1", "jit4", "jit2-7ctas", "jit1-1cta"])
+def test_dynamic_dispatch_matches_oracle(cuda_device, opts):
+    """Dynamic dispatch (tasks claimed by the CTAs at run time, stage by
+    stage) computes the same decoder: prompt and teacher-forced decode steps
+    against the oracle, with fine ranges, a reduced grid and a single CTA
+    that claims every task."""
+    import torch
+
+    plan, kv = harness.gpu_plan(TINY, 256, opts=mk.mk_plan_options(**opts))
+    model = harness.oracle_model(TINY)
+    harness.run_teacher_forced(plan, kv, model, synth.tokens(70, 0, 15, TINY.vocab), 5, 256)
+    t = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    logits = torch.empty((1, TINY.vocab), dtype=torch.float32, device=cuda_device)
+    st = mk.lib().mk_decode_step_ablation(plan.h, t.data_ptr(), t.data_ptr(), ctypes.byref(kv.desc),
+                                          logits.data_ptr(), None)
+    assert st == mk.MK_ERR_UNSUPPORTED  # one operator per launch needs the static queues
+
+
+def test_dynamic_dispatch_full_size_from_seeded_cache(cuda_device):
+    """The 8B-shaped decoder under dynamic dispatch, from a seeded cache."""
+    wl = WORKLOADS["8b"]
+    m = wl.model
+    ctx, steps = 100, 2
+    max_seq = ((ctx + steps + 64) // 64) * 64
+    plan, kv = harness.gpu_plan(m, max_seq, opts=mk.mk_plan_options(jit=1))
+    model = harness.oracle_model(m)
+    caches = harness.fill_synthetic_cache(kv, model, m, ctx, 1, max_seq)
+    harness.run_from_cache(plan, kv, model, caches, ctx, steps, synth.tokens(1, wl.seed, 0, m.vocab))

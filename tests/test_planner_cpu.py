@@ -253,3 +253,84 @@ def test_kv_append_graph_orders_append_between_qkv_and_attention(batch):
     att = [t for t in tasks if t.op == mk.OP_ATTN]
     kva_ev = {t.signal_event for t in kva}
     assert all(t.wait_event in kva_ev for t in att)
+
+
+def simulate_jit(tasks, n_events, n_ctas, seed, ring=8):
+    """Dynamic dispatch as the device runs it: each CTA claims the next
+    unclaimed task of the earliest stage with any left (at most `ring`
+    claimed and not yet released: a ring slot is reused only once its task
+    is released and taken), and runs its claims in claim order once each
+    one's event reaches its threshold; CTAs act in a random order."""
+    import random
+
+    rnd = random.Random(seed)
+    stages, cur = [], None
+    for t in tasks:  # stage = a run of tasks of one (layer, op)
+        if (t.layer, t.op) != cur:
+            stages.append([])
+            cur = (t.layer, t.op)
+        stages[-1].append(t)
+    nxt = [0] * len(stages)
+    stage = 0
+    claimed = defaultdict(list)
+    ctr = [0] * n_events
+    done_splits = defaultdict(int)
+    order, ran = [], 0
+    while ran < len(tasks):
+        progress = False
+        for c in rnd.sample(range(n_ctas), n_ctas):
+            if len(claimed[c]) < ring and stage < len(stages) and rnd.random() < 0.7:
+                while stage < len(stages) and nxt[stage] >= len(stages[stage]):
+                    stage += 1
+                if stage < len(stages):
+                    claimed[c].append(stages[stage][nxt[stage]])
+                    nxt[stage] += 1
+                    progress = True
+            if claimed[c]:
+                t = claimed[c][0]
+                if t.wait_event < 0 or ctr[t.wait_event] >= t.wait_count:
+                    claimed[c].pop(0)
+                    if t.op == mk.OP_ATTN:
+                        k = (t.layer, t.a0, t.a1)
+                        done_splits[k] += 1
+                        if done_splits[k] == t.a3:
+                            ctr[t.signal_event] += 1
+                    elif t.signal_event >= 0:
+                        ctr[t.signal_event] += 1
+                    order.append(t)
+                    ran += 1
+                    progress = True
+        if not progress:
+            return False, order
+    return True, order
+
+
+@pytest.mark.parametrize("jit,num_ctas,seed", [(1, 148, 0), (2, 148, 1), (4, 37, 2), (1, 5, 3)])
+def test_dynamic_dispatch_graph_completes_under_any_claim_order(jit, num_ctas, seed):
+    """Dynamic dispatch (options.jit): no task is bound to a CTA, stages are
+    contiguous in stage order, projections are cut into jit ranges per CTA,
+    and a randomised run of the claim-and-run rule drains every task with
+    the dependencies respected."""
+    m = SHAPES["8b"]
+    cfg = mk.model_cfg(m, 1, 1024)
+    tasks, n_events = mk.mk_plan_describe(cfg, num_ctas, mk.mk_plan_options(jit=jit))
+    assert all(t.cta == -1 for t in tasks)
+    qkv = [t for t in tasks if t.op == mk.OP_QKV and t.layer == 0]
+    rows = op_rows(m, mk.OP_QKV)
+    assert len(qkv) == min(rows, jit * num_ctas)
+    ok, order = simulate_jit(tasks, n_events, num_ctas, seed)
+    assert ok, "deadlock"
+    pos = defaultdict(list)
+    for i, t in enumerate(order):
+        pos[(t.layer, t.op)].append(i)
+    for l in range(m.n_layers):
+        assert min(pos[(l, mk.OP_ATTN)]) > max(pos[(l, mk.OP_QKV)])
+        assert min(pos[(l, mk.OP_O)]) > max(pos[(l, mk.OP_ATTN)])
+        assert min(pos[(l, mk.OP_GU)]) > max(pos[(l, mk.OP_O)])
+        assert min(pos[(l, mk.OP_DOWN)]) > max(pos[(l, mk.OP_GU)])
+
+
+def test_dynamic_dispatch_rejects_tracing():
+    cfg = mk.model_cfg(SHAPES["tiny"], 1, 128)
+    with pytest.raises(mk.MKError):
+        mk.mk_plan_describe(cfg, 148, mk.mk_plan_options(jit=1, trace=1))
