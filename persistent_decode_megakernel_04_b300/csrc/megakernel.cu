@@ -1719,6 +1719,251 @@ struct Consumer {
         return kv_elem((sl & 2) ? hi : lo, 0u, ts_log2, halves, kv, tok & ((1 << ts_log2) - 1), e);
     }
 
+    // Long context splits (G <= 4 query heads per kv head, at least four
+    // blocks): each step holds two 64-token blocks, and warp w takes tokens
+    // 16w..16w+15 of it through the whole computation in registers, with no
+    // barrier inside the step.  Scores S^T = K Q^T (m16n8k16, split-bf16
+    // queries as 2G columns); an online softmax over the warp's own tokens
+    // (running max and sum per head); the weights split into bf16 high and
+    // low parts, moved from the scores' accumulator layout to the B-operand
+    // layout by an 8x8 transpose (movmatrix); O^T[d][2G] += V^T P^T over all
+    // d rows.  After the last step the eight warps' (m, l, O) are merged in a
+    // three-round tree through shared memory, and the result is left where
+    // the per-block path leaves it: oacc (warp w: rows 16w.. of d, high
+    // columns; low columns 0) and att_m, att_l.
+    __device__ void attend_warps(const Ctx &c, const AttnRange &r, int layer, int G, int nks, int halves, int nsl,
+                                 int ts_log2, uint32_t qb, float (&oacc)[2][4]) {
+        SmemCtl *sc = c.sc;
+        const int tr = lane >> 2, cq = lane & 3;
+        const int partner = (G >= 2) ? G / 2 : 0;   // lane distance to the low-part column (G <= 4)
+        const bool head_lane = (G == 1) ? cq == 0 : cq < G / 2;
+        const bool pad_lane = (G == 2 && cq >= 2) || (G == 1 && cq != 0);
+        float o2[8][4];  // O^T rows 16 mt + tr (+8), columns 2 cq (+1): this warp's tokens
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) o2[mt][i] = 0.f;
+        float wm[2] = {-INFINITY, -INFINITY}, wl[2] = {0.f, 0.f};  // head lanes: heads 2cq, 2cq+1
+        const uint64_t tb0 = tracing ? globaltimer_ns() : 0;
+        for (int32_t blk = r.blo; blk < r.bhi; blk += 2) {
+            const int NB = (blk + 1 < r.bhi) ? 2 : 1;
+            const int nslots = NB * nsl;
+            const uint32_t sid0 = wait_slot_at(c, consumed);
+            const uint32_t sid1 = (nslots > 1) ? wait_slot_at(c, consumed + 1u) : sid0;
+            const uint32_t sid2 = (nslots > 2) ? wait_slot_at(c, consumed + 2u) : sid0;
+            const uint32_t sid3 = (nslots > 3) ? wait_slot_at(c, consumed + 3u) : sid0;
+            const uint32_t sb0 = smem_u32(c.ring + (size_t)sid0 * slot_bytes);
+            const uint32_t sb1 = smem_u32(c.ring + (size_t)sid1 * slot_bytes);
+            const uint32_t sb2 = smem_u32(c.ring + (size_t)sid2 * slot_bytes);
+            const uint32_t sb3 = smem_u32(c.ring + (size_t)sid3 * slot_bytes);
+            const int32_t tok0 = blk * kAttnBlock;
+            if (wc < 4 * NB) {
+                float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    if (ks < nks) {
+                        uint32_t a[4], qf[2];
+                        ldsm_x4(a, kv_elem4(sb0, sb1, sb2, sb3, ts_log2, halves, 0, 16 * wc + (lane & 15),
+                                            ks * 16 + (lane >> 4) * 8));
+                        ldsm_x2(qf, qb + (uint32_t)(((lane & 7) * kQhlStride + ks * 16 + ((lane >> 3) & 1) * 8) * 2));
+                        mma_bf16_16816(sacc, a, qf);
+                    }
+                }
+                // scores of (token row, head) in the head lanes; -inf past the context
+                float sv[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float v = sacc[i];
+                    if (G == 1) v = (i & 1) ? 0.f : sacc[i] + sacc[i + 1];
+                    else v += __shfl_xor_sync(0xFFFFFFFFu, v, partner);
+                    const int tok = 16 * wc + tr + (i >> 1) * 8;
+                    sv[i] = (tok0 + tok < r.ctx) ? v : -INFINITY;
+                }
+                // the step's maximum per head over this warp's 16 tokens
+                float mx[2] = {fmaxf(sv[0], sv[2]), fmaxf(sv[1], sv[3])};
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int o = 4; o < 32; o <<= 1) mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xFFFFFFFFu, mx[j], o));
+                float alpha[2], nm[2];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    nm[j] = fmaxf(wm[j], mx[j]);
+                    alpha[j] = (nm[j] == -INFINITY || wm[j] == -INFINITY) ? (nm[j] == -INFINITY ? 1.f : 0.f)
+                                                                         : expf(wm[j] - nm[j]);
+                }
+                float pv[4], ps[2] = {0.f, 0.f};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    pv[i] = (sv[i] == -INFINITY) ? 0.f : expf(sv[i] - nm[i & 1]);
+                    ps[i & 1] += pv[i];
+                }
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+#pragma unroll
+                    for (int o = 4; o < 32; o <<= 1) ps[j] += __shfl_xor_sync(0xFFFFFFFFu, ps[j], o);
+                    wl[j] = wl[j] * alpha[j] + ps[j];
+                    wm[j] = nm[j];
+                }
+                // rescale this warp's O: each lane's columns belong to its own
+                // heads (high parts) or to its partner's (low parts)
+                float ca0 = alpha[0], ca1 = alpha[1];
+                if (G >= 2) {
+                    const float r0 = __shfl_xor_sync(0xFFFFFFFFu, alpha[0], partner);
+                    const float r1 = __shfl_xor_sync(0xFFFFFFFFu, alpha[1], partner);
+                    if (!head_lane) {
+                        ca0 = r0;
+                        ca1 = r1;
+                    }
+                } else {
+                    ca1 = alpha[0];  // G = 1: columns 0 and 1 are head 0's high and low parts
+                }
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) {
+                    o2[mt][0] *= ca0;
+                    o2[mt][1] *= ca1;
+                    o2[mt][2] *= ca0;
+                    o2[mt][3] *= ca1;
+                }
+                // the weights as the B operand P^T[16 tokens][2G columns]:
+                // high parts in the head lanes' columns, low parts in their
+                // partners', bf16 pairs transposed 8x8
+                float hi[4], lo[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    hi[i] = __uint_as_float((uint32_t)f32_to_bf16_bits(pv[i]) << 16);
+                    lo[i] = pv[i] - hi[i];
+                }
+                float val[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if (G == 1) {
+                        val[i] = (i & 1) ? lo[i - 1] : hi[i];
+                    } else {
+                        const float lr = __shfl_xor_sync(0xFFFFFFFFu, lo[i], partner);
+                        val[i] = head_lane ? hi[i] : lr;
+                    }
+                    if (pad_lane) val[i] = 0.f;
+                }
+                const uint32_t r0 = (uint32_t)f32_to_bf16_bits(val[0]) | ((uint32_t)f32_to_bf16_bits(val[1]) << 16);
+                const uint32_t r1 = (uint32_t)f32_to_bf16_bits(val[2]) | ((uint32_t)f32_to_bf16_bits(val[3]) << 16);
+                const uint32_t b[2] = {movmatrix_trans(r0), movmatrix_trans(r1)};
+                const int q = lane >> 3;
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) {
+                    if (mt < nks) {
+                        uint32_t a[4];
+                        ldsm_x4_trans(a, kv_elem4(sb0, sb1, sb2, sb3, ts_log2, halves, 1,
+                                                  16 * wc + (q >> 1) * 8 + (lane & 7), 16 * mt + (q & 1) * 8));
+                        mma_bf16_16816(o2[mt], a, b);
+                    }
+                }
+            }
+            compute_bar();  // the step's slots are free
+            if (ct == 0) {
+                const uint32_t na = c.p->tc ? 1u : (uint32_t)kComputeWarps;
+                mbar_arrive_n(&sc->empty[sid0], na);
+                if (nslots > 1) mbar_arrive_n(&sc->empty[sid1], na);
+                if (nslots > 2) mbar_arrive_n(&sc->empty[sid2], na);
+                if (nslots > 3) mbar_arrive_n(&sc->empty[sid3], na);
+            }
+            consumed += (uint32_t)nslots;
+        }
+        // the head lanes' per-head O: high plus low column
+        float oh[8][4];
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float v = o2[mt][i];
+                if (G == 1) v = (i & 1) ? 0.f : o2[mt][i] + o2[mt][i + 1];
+                else v += __shfl_xor_sync(0xFFFFFFFFu, v, partner);
+                oh[mt][i] = v;
+            }
+        // tree merge of the warps' (m, l, O) through shared memory: warps
+        // 4..7 into 0..3, 2..3 into 0..1, 1 into 0
+        float *mo = &sc->at.s_s[0][0];       // [4][kMaxHeadDim][4] partial O
+        float *mm = mo + 4 * kMaxHeadDim * 4;  // [4][4] running max
+        float *ml = mm + 16;                   // [4][4] sum
+        const int dd = nks * 16;
+        for (int half = 4; half >= 1; half >>= 1) {
+            if (wc >= half && wc < 2 * half && head_lane) {
+                const int slot = wc - half;
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int h = (G == 1) ? 0 : 2 * cq + (i & 1);
+                        if (mt < nks && (G != 1 || (i & 1) == 0))
+                            mo[(slot * kMaxHeadDim + 16 * mt + tr + (i >> 1) * 8) * 4 + h] = oh[mt][i];
+                    }
+                if (tr == 0) {
+                    const int h0 = (G == 1) ? 0 : 2 * cq;
+                    mm[slot * 4 + h0] = wm[0];
+                    ml[slot * 4 + h0] = wl[0];
+                    if (G != 1) {
+                        mm[slot * 4 + h0 + 1] = wm[1];
+                        ml[slot * 4 + h0 + 1] = wl[1];
+                    }
+                }
+            }
+            compute_bar();
+            if (wc < half && head_lane) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    if (G == 1 && j == 1) continue;
+                    const int h = (G == 1) ? 0 : 2 * cq + j;
+                    const float mb = mm[wc * 4 + h], lb = ml[wc * 4 + h];
+                    const float M = fmaxf(wm[j], mb);
+                    const float wa = (wm[j] == -INFINITY) ? 0.f : expf(wm[j] - M);
+                    const float wb = (mb == -INFINITY) ? 0.f : expf(mb - M);
+#pragma unroll
+                    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+                        for (int i = j; i < 4; i += 2)
+                            if (mt < nks)
+                                oh[mt][i] = oh[mt][i] * wa +
+                                            mo[(wc * kMaxHeadDim + 16 * mt + tr + (i >> 1) * 8) * 4 + h] * wb;
+                    wl[j] = wl[j] * wa + lb * wb;
+                    wm[j] = M;
+                }
+            }
+            compute_bar();
+        }
+        // warp 0 holds the split's result: per-head O to shared memory, then
+        // every warp takes its rows of d in the per-block path's layout
+        if (wc == 0 && head_lane) {
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int h = (G == 1) ? 0 : 2 * cq + (i & 1);
+                    if (mt < nks && (G != 1 || (i & 1) == 0)) mo[(16 * mt + tr + (i >> 1) * 8) * 4 + h] = oh[mt][i];
+                }
+            if (tr == 0) {
+                const int h0 = (G == 1) ? 0 : 2 * cq;
+                sc->att_m[h0] = wm[0];
+                sc->att_l[h0] = wl[0];
+                if (G != 1) {
+                    sc->att_m[h0 + 1] = wm[1];
+                    sc->att_l[h0 + 1] = wl[1];
+                }
+            }
+        }
+        compute_bar();
+        if (wc < nks) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int col = 2 * cq + (i & 1);
+                const int e = 16 * wc + tr + (i >> 1) * 8;
+                oacc[0][i] = (col < G && e < dd) ? mo[e * 4 + col] : 0.f;
+                oacc[1][i] = 0.f;
+            }
+        }
+        compute_bar();  // the merge buffer (the scores' scratch) is free
+        if (tracing) act_wait_ns += globaltimer_ns() - tb0;
+    }
+
     __device__ void run_attn(const Ctx &c, const Task &t) {
         const KParams &p = *c.p;
         SmemCtl *sc = c.sc;
@@ -1939,11 +2184,16 @@ struct Consumer {
                 acc_wait_ns += globaltimer_ns() - tb2;  // value sums
             }
         };
-        // pairs of blocks while the ring can hold both at once, then the rest
-        int32_t blk = r.blo;
-        if (ns >= (uint32_t)(2 * nsl))
-            for (; blk + 1 < r.bhi; blk += 2) attend(std::integral_constant<int, 2>{}, blk);
-        for (; blk < r.bhi; ++blk) attend(std::integral_constant<int, 1>{}, blk);
+        if (G <= 4 && r.bhi - r.blo >= 4 && ns >= (uint32_t)(2 * nsl)) {
+            // long splits: every warp runs its own tokens end to end
+            attend_warps(c, r, t.layer, G, nks, halves, nsl, ts_log2, qb, oacc);
+        } else {
+            // pairs of blocks while the ring can hold both at once, then the rest
+            int32_t blk = r.blo;
+            if (ns >= (uint32_t)(2 * nsl))
+                for (; blk + 1 < r.bhi; blk += 2) attend(std::integral_constant<int, 2>{}, blk);
+            for (; blk < r.bhi; ++blk) attend(std::integral_constant<int, 1>{}, blk);
+        }
         if (r.has_new) {
             // the new token, from shared memory: one more online-softmax step
             if (wc < G) {

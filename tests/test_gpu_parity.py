@@ -438,3 +438,25 @@ def test_dynamic_dispatch_full_size_from_seeded_cache(cuda_device):
     model = harness.oracle_model(m)
     caches = harness.fill_synthetic_cache(kv, model, m, ctx, 1, max_seq)
     harness.run_from_cache(plan, kv, model, caches, ctx, steps, synth.tokens(1, wl.seed, 0, m.vocab))
+
+
+@pytest.mark.parametrize("m", [WORKLOADS["tiny"].model, synth.TINY_MHA, synth.TINY_D128, synth.TINY_G8],
+                         ids=["g2", "mha", "d128-g4", "g8"])
+@pytest.mark.parametrize("batch", [1, 3])
+def test_long_splits_warp_local_attention(cuda_device, m, batch):
+    """Splits of four or more cached blocks run attention warp by warp (each
+    warp its own tokens: scores, online softmax and value sums in registers,
+    then a tree merge of the warps); one split per head over a 300-token
+    prompt (five blocks: two two-block steps and a one-block step) for GQA
+    groups of 2, 1 and 4 (head_dim 128), and 8, which keeps the per-block
+    path."""
+    from tests.test_gpu_batched import prompts
+
+    max_seq = 384
+    plan, kv = harness.gpu_plan(m, max_seq, batch=batch, opts=mk.mk_plan_options(attn_splits=1))
+    model = harness.oracle_model(m)
+    if batch == 1:
+        harness.run_teacher_forced(plan, kv, model, synth.tokens(300, 0, 16, m.vocab), 4, max_seq)
+    else:
+        harness.run_teacher_forced_batch(plan, kv, model, prompts(batch, 300, seed=11, vocab=m.vocab), 3, max_seq,
+                                         rows=[0, batch - 1])
