@@ -1508,7 +1508,10 @@ struct Consumer {
                 epi_bar();
                 last = sc->ep_last != 0u;
             }
-            if (last) finish_tile(c, t, g, mats, tile, r, tq, whole, cf, cl, rc);
+            if (last) {
+                if (mats == 2) finish_tile<2>(c, t, g, tile, r, tq, whole, cf, cl, rc);
+                else finish_tile<1>(c, t, g, tile, r, tq, whole, cf, cl, rc);
+            }
             tc_fence_before();
             epi_bar();
             if (et == 0) mbar_arrive(&sc->acc_empty[ab]);
@@ -1530,8 +1533,12 @@ struct Consumer {
         return p.part + ((size_t)rc * 2 + sidx) * 2 * (size_t)p.npad * kTcTileM;
     }
 
-    __device__ void finish_tile(const Ctx &c, const Task &t, const TcGeom &g, int mats, int32_t tile, int r,
-                                uint32_t tq, bool whole, int32_t cf, int32_t cl, int32_t rc) {
+    // MATS (1, or 2 for gate/up) is a template argument: the gate/up tile's
+    // second accumulator is not held live in the single-matrix epilogues.
+    template <int MATS>
+    __device__ void finish_tile(const Ctx &c, const Task &t, const TcGeom &g, int32_t tile, int r, uint32_t tq,
+                                bool whole, int32_t cf, int32_t cl, int32_t rc) {
+        constexpr int mats = MATS;
         const KParams &p = *c.p;
         SmemCtl *sc = c.sc;
         const int op = t.op;
@@ -1560,26 +1567,48 @@ struct Consumer {
                                               : (t.layer + 1 < p.L ? p.layers[t.layer + 1].attn_norm : p.final_norm);
             gain = __uint_as_float((uint32_t)gv[orow] << 16);
         }
+        const bool resid = (op == OP_O || op == OP_DOWN);
         for (int c0 = 0; c0 < p.npad; c0 += 16) {
-            float v[2][16];
+            // the residual stream's values are read before the partial sums,
+            // all independent loads, so that one round trip covers them
+            float xo[16];
+            if (resid) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    xo[i] = (c0 + i < p.B && row_ok) ? __ldcg(p.x + (size_t)(c0 + i) * p.H + orow) : 0.f;
+            }
+            float v[mats][16];
+#pragma unroll
             for (int m = 0; m < mats; ++m) {
                 if (whole) {
                     tmem_ld_split16(tq + (uint32_t)(m * 2 * p.npad + c0), p.npad, v[m]);
                 } else {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) v[m][i] = 0.f;
-                    for (int32_t cc = cf; cc <= cl; ++cc) {
-                        if (!range_nonempty(cc, g.units, p.num_ctas)) continue;
-                        float w[16];
-                        if (cc == rc) {
-                            tmem_ld_split16(tq + (uint32_t)(m * 2 * p.npad + c0), p.npad, w);
-                        } else {
-                            const float *src = part_ptr(p, cc, tile, g) + ((size_t)m * p.npad + c0) * kTcTileM + r;
+                    // kFix contributing ranges' partial sums are loaded at once, then
+                    // added in range order (the same sums, fewer round trips; more
+                    // than two at once spills registers)
+                    constexpr int kFix = 2;
+                    for (int32_t cg = cf; cg <= cl; cg += kFix) {
+                        float w[kFix][16];
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) w[i] = __ldcg(src + (size_t)i * kTcTileM);
+                        for (int j = 0; j < kFix; ++j) {
+                            const int32_t cc = cg + j;
+                            if (cc == rc) {
+                                tmem_ld_split16(tq + (uint32_t)(m * 2 * p.npad + c0), p.npad, w[j]);
+                            } else if (cc <= cl && range_nonempty(cc, g.units, p.num_ctas)) {
+                                const float *src = part_ptr(p, cc, tile, g) + ((size_t)m * p.npad + c0) * kTcTileM + r;
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) w[j][i] = __ldcg(src + (size_t)i * kTcTileM);
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) w[j][i] = 0.f;
+                            }
                         }
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) v[m][i] += w[i];
+                        for (int j = 0; j < kFix; ++j)
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) v[m][i] += w[j][i];
                     }
                 }
             }
@@ -1594,21 +1623,21 @@ struct Consumer {
                     case OP_O:
                     case OP_DOWN: {
                         const size_t xi = (size_t)b * p.H + orow;
-                        const float xn = __ldcg(p.x + xi) + v[0][i];
+                        const float xn = xo[i] + v[0][i];
                         p.x[xi] = xn;
                         store_split(p.xa, p.H, p.npad, b, orow, gain * xn);
                         sq[i] = xn * xn;
                         break;
                     }
                     case OP_GU: {
-                        const float gg = sc->rs[b] * v[0][i], uu = sc->rs[b] * v[1][i];
+                        const float gg = sc->rs[b] * v[0][i], uu = sc->rs[b] * v[mats - 1][i];
                         store_split(p.h_a, p.I, p.npad, b, orow, gg / (1.f + expf(-gg)) * uu);
                         break;
                     }
                     default: p.logits[(size_t)b * p.V + orow] = sc->rs[b] * v[0][i]; break;
                 }
             }
-            if (op == OP_O || op == OP_DOWN) {
+            if (resid) {
                 // per-warp sums of x^2 for the 16 sequences of this chunk
                 const float s16 = warp_reduce16(sq, lane);
                 if ((lane & 1) == 0) sc->ssq_red[q4][c0 + ((lane >> 1) & 15)] = s16;
