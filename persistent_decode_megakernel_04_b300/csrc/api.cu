@@ -58,6 +58,7 @@ struct mk_plan {
     mk_kv_cache kv_seen{};
     bool kv_maps_valid = false;
     alignas(64) uint8_t kv_maps[2][128];
+    int32_t kv_halves_3d = 0;
 };
 
 namespace mk {
@@ -93,11 +94,35 @@ bool encode_bf16_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t o
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A pool of d = 128 as a 3-D view (column within a 64-column half, token
+// row, half): one box of 64 columns x ts tokens x 2 halves lands in shared
+// memory as the two 128-byte-swizzled half tiles one after the other, the
+// layout two 2-D copies would give, in one copy.
+bool encode_kv_halves(CUtensorMap *m, const void *base, uint64_t rows, uint32_t ts) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {64, rows, 2};
+    const cuuint64_t strides[2] = {256, 128};
+    const cuuint32_t box[3] = {64, ts, 2};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // K and V pools as [L * num_pages * nkv * page_size][d] bf16 rows, read in
-// boxes of 64 columns x ts tokens.
+// boxes of 64 columns x ts tokens (d = 64), or of both halves of d = 128 at
+// once where the driver takes the 3-D view (kv_halves_3d), else per half.
 bool encode_kv_maps(KParams &k, const mk_model_cfg &c, const mk_kv_cache &kv, int32_t ts) {
     const uint64_t rows = (uint64_t)c.n_layers * kv.num_pages * c.n_kv_heads * c.page_size;
     if (rows >= (1ull << 31)) return false;
+    k.kv_halves_3d = 0;
+    if (c.head_dim == 128 &&
+        encode_kv_halves(reinterpret_cast<CUtensorMap *>(k.kv_maps[0]), kv.k_pool, rows, (uint32_t)ts) &&
+        encode_kv_halves(reinterpret_cast<CUtensorMap *>(k.kv_maps[1]), kv.v_pool, rows, (uint32_t)ts)) {
+        k.kv_halves_3d = 1;
+        return true;
+    }
     return encode_bf16_2d(reinterpret_cast<CUtensorMap *>(k.kv_maps[0]), kv.k_pool, c.head_dim, rows, ts) &&
            encode_bf16_2d(reinterpret_cast<CUtensorMap *>(k.kv_maps[1]), kv.v_pool, c.head_dim, rows, ts);
 }
@@ -167,6 +192,7 @@ mk_status check_kv(mk_plan *p, const mk_kv_cache *kv) {
     p->kv_maps_valid = false;
     if (!encode_kv_maps(probe, p->cfg, *kv, p->tables.g.tps)) return MK_ERR_INVALID;  // pools too large for a map
     std::memcpy(p->kv_maps, probe.kv_maps, sizeof(p->kv_maps));
+    p->kv_halves_3d = probe.kv_halves_3d;
     p->kv_seen = *kv;
     p->kv_maps_valid = true;
     return MK_OK;
@@ -191,6 +217,7 @@ KParams step_params(const mk_plan *p, const int32_t *tokens, int32_t tok_stride,
                     int32_t pos_stride, const mk_kv_cache *kv, float *logits) {
     KParams k = p->base;
     std::memcpy(k.kv_maps, p->kv_maps, sizeof(k.kv_maps));  // encoded by check_kv
+    k.kv_halves_3d = p->kv_halves_3d;
     k.k_pool = static_cast<uint16_t *>(kv->k_pool);
     k.v_pool = static_cast<uint16_t *>(kv->v_pool);
     k.page_table = kv->page_table;

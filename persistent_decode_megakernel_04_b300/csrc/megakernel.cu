@@ -565,6 +565,13 @@ struct Producer {
                 uint32_t s;
                 if (!begin_slot(c, &s, (uint32_t)(2 * halves * ts * 128))) return false;
                 uint8_t *dst = c.ring + (size_t)s * slot_bytes;
+                if (p.kv_halves_3d) {
+                    tma_load_3d(dst, p.kv_maps[0], 0, row0 + j * ts, 0, &c.sc->full[s], pol);
+                    tma_load_3d(dst + (size_t)halves * ts * 128, p.kv_maps[1], 0, row0 + j * ts, 0, &c.sc->full[s],
+                                pol);
+                    ++issued;
+                    continue;
+                }
                 for (int h = 0; h < halves; ++h) {
                     tma_load_2d(dst + (size_t)h * ts * 128, p.kv_maps[0], h * 64, row0 + j * ts, &c.sc->full[s], pol);
                     tma_load_2d(dst + (size_t)(halves + h) * ts * 128, p.kv_maps[1], h * 64, row0 + j * ts,

@@ -86,6 +86,7 @@ struct KParams {
     // TMA maps of the K and V pools seen as [L*num_pages*nkv*page_size][d]
     // bf16 rows, boxes of 64 columns x attn_ts rows, 128-byte swizzled
     alignas(64) uint8_t kv_maps[2][128];
+    int32_t kv_halves_3d;  // kv_maps are 3-D views copying both 64-column halves of d = 128 at once
     // batched (tensor-core) path
     int32_t tc;              // nonzero: projections run as tcgen05 tiles
     int32_t npad;            // MMA N: batch rounded up to 16
