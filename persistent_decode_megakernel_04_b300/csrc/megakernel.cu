@@ -1780,28 +1780,39 @@ struct Consumer {
 #pragma unroll
             for (int i = 0; i < 4; ++i) o2[mt][i] = 0.f;
         float wm[2] = {-INFINITY, -INFINITY}, wl[2] = {0.f, 0.f};  // head lanes: heads 2cq, 2cq+1
+        // This warp's 16 tokens of a step lie in one slot (the step's slot
+        // wsl); the ldmatrix addresses of its K and V fragments within that
+        // slot are the same every step, so they are computed once here:
+        // kof[ks] (K rows 16 wc + lane % 16, columns 16 ks + 8 (lane / 16))
+        // and vof[mt] (V rows 16 wc + 8 (q / 2) + lane % 8, columns 16 mt +
+        // 8 (q % 2), q = lane / 8).
+        const int wsl = (16 * wc) >> ts_log2;
+        uint32_t kof[8], vof[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            kof[j] = kv_elem(0u, 0u, ts_log2, halves, 0, (16 * wc + (lane & 15)) & ((1 << ts_log2) - 1),
+                             j * 16 + (lane >> 4) * 8);
+            const int q = lane >> 3;
+            vof[j] = kv_elem(0u, 0u, ts_log2, halves, 1, (16 * wc + (q >> 1) * 8 + (lane & 7)) & ((1 << ts_log2) - 1),
+                             16 * j + (q & 1) * 8);
+        }
+        const uint32_t qlane = qb + (uint32_t)(((lane & 7) * kQhlStride + ((lane >> 3) & 1) * 8) * 2);
         const uint64_t tb0 = tracing ? globaltimer_ns() : 0;
         for (int32_t blk = r.blo; blk < r.bhi; blk += 2) {
             const int NB = (blk + 1 < r.bhi) ? 2 : 1;
             const int nslots = NB * nsl;
-            const uint32_t sid0 = wait_slot_at(c, consumed);
-            const uint32_t sid1 = (nslots > 1) ? wait_slot_at(c, consumed + 1u) : sid0;
-            const uint32_t sid2 = (nslots > 2) ? wait_slot_at(c, consumed + 2u) : sid0;
-            const uint32_t sid3 = (nslots > 3) ? wait_slot_at(c, consumed + 3u) : sid0;
-            const uint32_t sb0 = smem_u32(c.ring + (size_t)sid0 * slot_bytes);
-            const uint32_t sb1 = smem_u32(c.ring + (size_t)sid1 * slot_bytes);
-            const uint32_t sb2 = smem_u32(c.ring + (size_t)sid2 * slot_bytes);
-            const uint32_t sb3 = smem_u32(c.ring + (size_t)sid3 * slot_bytes);
             const int32_t tok0 = blk * kAttnBlock;
             if (wc < 4 * NB) {
+                // only this warp's slot: every slot of the step is released
+                // together after the barrier below, so no warp runs a lap ahead
+                const uint32_t sbw = smem_u32(c.ring + (size_t)wait_slot_at(c, consumed + (uint32_t)wsl) * slot_bytes);
                 float sacc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     if (ks < nks) {
                         uint32_t a[4], qf[2];
-                        ldsm_x4(a, kv_elem4(sb0, sb1, sb2, sb3, ts_log2, halves, 0, 16 * wc + (lane & 15),
-                                            ks * 16 + (lane >> 4) * 8));
-                        ldsm_x2(qf, qb + (uint32_t)(((lane & 7) * kQhlStride + ks * 16 + ((lane >> 3) & 1) * 8) * 2));
+                        ldsm_x4(a, sbw + kof[ks]);
+                        ldsm_x2(qf, qlane + (uint32_t)(ks * 32));
                         mma_bf16_16816(sacc, a, qf);
                     }
                 }
@@ -1884,13 +1895,11 @@ struct Consumer {
                 const uint32_t r0 = (uint32_t)f32_to_bf16_bits(val[0]) | ((uint32_t)f32_to_bf16_bits(val[1]) << 16);
                 const uint32_t r1 = (uint32_t)f32_to_bf16_bits(val[2]) | ((uint32_t)f32_to_bf16_bits(val[3]) << 16);
                 const uint32_t b[2] = {movmatrix_trans(r0), movmatrix_trans(r1)};
-                const int q = lane >> 3;
 #pragma unroll
                 for (int mt = 0; mt < 8; ++mt) {
                     if (mt < nks) {
                         uint32_t a[4];
-                        ldsm_x4_trans(a, kv_elem4(sb0, sb1, sb2, sb3, ts_log2, halves, 1,
-                                                  16 * wc + (q >> 1) * 8 + (lane & 7), 16 * mt + (q & 1) * 8));
+                        ldsm_x4_trans(a, sbw + vof[mt]);
                         mma_bf16_16816(o2[mt], a, b);
                     }
                 }
@@ -1898,10 +1907,7 @@ struct Consumer {
             compute_bar();  // the step's slots are free
             if (ct == 0) {
                 const uint32_t na = c.p->tc ? 1u : (uint32_t)kComputeWarps;
-                mbar_arrive_n(&sc->empty[sid0], na);
-                if (nslots > 1) mbar_arrive_n(&sc->empty[sid1], na);
-                if (nslots > 2) mbar_arrive_n(&sc->empty[sid2], na);
-                if (nslots > 3) mbar_arrive_n(&sc->empty[sid3], na);
+                for (int j = 0; j < nslots; ++j) mbar_arrive_n(&sc->empty[(consumed + (uint32_t)j) % ns], na);
             }
             consumed += (uint32_t)nslots;
         }
