@@ -71,6 +71,7 @@ struct SmemCtl {
     // dynamic dispatch: the tasks this CTA's scheduler claimed, a ring of
     // task indices (the i-th claimed task in slot i % kJitRing)
     uint32_t jq[kJitRing];
+    uint32_t jmma;  // dynamic dispatch: claims the MMA warp has read
     uint32_t jclaimed;   // tasks claimed so far
     uint32_t jdone;      // 1 once every stage is exhausted (jclaimed is final)
     uint32_t jprod;      // claimed tasks the producer has read
@@ -777,7 +778,8 @@ __device__ __noinline__ void scheduler_loop_jit(const Ctx &c, ActProducer &ap) {
             // a slot is free once the producer and the compute warps have
             // read its task and this scheduler has released it
             const uint32_t jcomp = ld_acquire_cta(&sc->jcomp);
-            const uint32_t behind = min(min(ld_acquire_cta(&sc->jprod), jcomp), released);
+            uint32_t behind = min(min(ld_acquire_cta(&sc->jprod), jcomp), released);
+            if (p.tc) behind = min(behind, ld_acquire_cta(&sc->jmma));
             if (claimed - behind >= (uint32_t)kJitRing) return false;
             // claim only kJitAhead tasks beyond the one the compute warps hold:
             // a CTA that claimed far ahead would keep later stages' tasks from
@@ -885,7 +887,7 @@ __device__ __forceinline__ void compute_bar() { named_bar_sync(1, kComputeThread
 // warp takes the same branch on it.
 __device__ __forceinline__ bool compute_bar_or(bool v) { return named_bar_or(1, kComputeThreads, v); }
 // Barrier of the four epilogue warps of the batched path.
-constexpr int kEpiThreads = 128;
+constexpr int kEpiThreads = kComputeThreads;  // the batched epilogue runs on every compute warp
 __device__ __forceinline__ void epi_bar() { named_bar_sync(2, kEpiThreads); }
 
 // Sums 8 per-lane values over the warp and scatters the result: lane l
@@ -1389,26 +1391,44 @@ struct Consumer {
     }
 
     // ------------------------------------------ batched path: projections
-    // Units [a0, a1) of the operator, cut by row tile into segments.  Compute
-    // warp 0, lane 0 issues the MMAs of each segment into one of two TMEM
-    // accumulator buffers; compute warps 2..5 (TMEM lane quarters 0..3) read
-    // them back and run the fused epilogue; the other compute warps idle.
+    // Units [a0, a1) of the operator, cut by row tile into segments.  The MMA
+    // warp issues the MMAs of each segment into one of two TMEM accumulator
+    // buffers (mma_role); the eight compute warps read them back and run the
+    // fused epilogue, two warps per TMEM lane quarter (warp id mod 4), each
+    // of the pair on alternate 16-column chunks.
     __device__ void run_gemm(const Ctx &c, const Task &t) {
         const KParams &p = *c.p;
         const TcGeom g = p.tcg[t.op];
         const int mats = (t.op == OP_GU) ? 2 : 1;
         const int32_t t0 = t.a0 / g.kchunks, t1 = (t.a1 - 1) / g.kchunks;
-        const bool issuer = (wc == 0 && lane == 0);
-        if (issuer) mma_issuer(c, t, g, mats, t0, t1);
-        else if (wc >= 2 && wc < 6) epilogue(c, t, g, mats, t0, t1);
-        if (!issuer) {
-            consumed += (uint32_t)((t.a1 - t.a0) * mats);
-            aconsumed += (uint32_t)(t.a1 - t.a0);
-        }
+        epilogue(c, t, g, mats, t0, t1);
+        consumed += (uint32_t)((t.a1 - t.a0) * mats);
+        aconsumed += (uint32_t)(t.a1 - t.a0);
         seg += (uint32_t)(t1 - t0 + 1);
     }
 
-    __device__ void mma_issuer(const Ctx &c, const Task &t, const TcGeom &g, int mats, int32_t t0, int32_t t1) {
+    // The MMA warp's share of a projection task (one thread): issue its
+    // segments, advance the ring counters, record its waits in the trace.
+    __device__ bool mma_task(const Ctx &c, const Task &t, uint64_t *tr) {
+        const KParams &p = *c.p;
+        const TcGeom g = p.tcg[t.op];
+        const int mats = (t.op == OP_GU) ? 2 : 1;
+        const int32_t t0 = t.a0 / g.kchunks, t1 = (t.a1 - 1) / g.kchunks;
+        const uint32_t c0 = consumed, a0 = aconsumed;
+        const bool ok = mma_issuer(c, t, g, mats, t0, t1);
+        consumed = c0 + (uint32_t)((t.a1 - t.a0) * mats);
+        aconsumed = a0 + (uint32_t)(t.a1 - t.a0);
+        seg += (uint32_t)(t1 - t0 + 1);
+        if (tr) {
+            tr[3] = full_wait_ns;
+            tr[6] = act_wait_ns;
+            tr[7] = acc_wait_ns;
+            full_wait_ns = act_wait_ns = acc_wait_ns = 0;
+        }
+        return ok;
+    }
+
+    __device__ bool mma_issuer(const Ctx &c, const Task &t, const TcGeom &g, int mats, int32_t t0, int32_t t1) {
         const KParams &p = *c.p;
         SmemCtl *sc = c.sc;
         const uint32_t nas = (uint32_t)p.num_aslots;
@@ -1418,7 +1438,7 @@ struct Consumer {
             const int32_t khi = (tile == t1) ? (t.a1 - 1) % g.kchunks + 1 : g.kchunks;
             const uint32_t ab = sg & 1u, use = sg >> 1;
             uint64_t t0 = tracing ? globaltimer_ns() : 0;
-            if (!wait_mbar(c, &sc->acc_empty[ab], (use & 1u) ^ 1u, SITE_ACC_WAIT)) return;
+            if (!wait_mbar(c, &sc->acc_empty[ab], (use & 1u) ^ 1u, SITE_ACC_WAIT)) return false;
             if (tracing) acc_wait_ns += globaltimer_ns() - t0;
             tc_fence_after();
             const uint32_t dcol = sc->tmem_base + ab * 4u * (uint32_t)p.npad;
@@ -1427,7 +1447,7 @@ struct Consumer {
                 if (tracing) t0 = globaltimer_ns();
                 for (int m = 0; m < mats; ++m) {
                     ws[m] = consumed % ns;
-                    if (!wait_mbar(c, &sc->full[ws[m]], (consumed / ns) & 1u, SITE_FULL_WAIT)) return;
+                    if (!wait_mbar(c, &sc->full[ws[m]], (consumed / ns) & 1u, SITE_FULL_WAIT)) return false;
                     ++consumed;
                 }
                 if (tracing) {
@@ -1436,7 +1456,7 @@ struct Consumer {
                     t0 = t1;
                 }
                 const uint32_t as = aconsumed % nas;
-                if (!wait_mbar(c, &sc->afull[as], (aconsumed / nas) & 1u, SITE_FULL_WAIT)) return;
+                if (!wait_mbar(c, &sc->afull[as], (aconsumed / nas) & 1u, SITE_FULL_WAIT)) return false;
                 ++aconsumed;
                 if (tracing) act_wait_ns += globaltimer_ns() - t0;
                 tc_fence_after();
@@ -1453,6 +1473,7 @@ struct Consumer {
             }
             umma_commit(&sc->acc_full[ab]);
         }
+        return true;
     }
 
     // Epilogue warps: for each segment, wait for its accumulator, publish or
@@ -1463,7 +1484,8 @@ struct Consumer {
         const int op = t.op;
         const int q4 = (wc + 2) & 3;  // TMEM lane quarter of this warp (its warp id mod 4)
         const int r = q4 * 32 + lane; // row of the tile held by this thread
-        const int et = ct - 64;       // 0..127
+        const int et = ct;            // 0..255
+        const int cfirst = 16 * (wc >> 2);  // this warp's first 16-column chunk; it takes every other one
         if (op == OP_QKV || op == OP_GU || op == OP_LM) {
             // RMSNorm scale of each sequence from the producers' per-tile sums of x^2
             for (int b = et; b < p.B; b += kEpiThreads) {
@@ -1495,7 +1517,7 @@ struct Consumer {
                 cl = range_of(tu0 + g.kchunks - 1, U, NR);
                 float *mine = part_ptr(p, rc, tile, g);
                 for (int m = 0; m < mats; ++m)
-                    for (int c0 = 0; c0 < p.npad; c0 += 16) {
+                    for (int c0 = cfirst; c0 < p.npad; c0 += 32) {
                         float v[16];
                         tmem_ld_split16(tq + (uint32_t)(m * 2 * p.npad + c0), p.npad, v);
 #pragma unroll
@@ -1550,7 +1572,7 @@ struct Consumer {
         SmemCtl *sc = c.sc;
         const int op = t.op;
         const int q4 = (wc + 2) & 3;
-        const int et = ct - 64;
+        const int et = ct;
         // where this thread's row goes
         int32_t orow = tile * kTcTileM + r, obase = 0, olim = g.rows;
         if (op == OP_QKV) {
@@ -1575,7 +1597,7 @@ struct Consumer {
             gain = __uint_as_float((uint32_t)gv[orow] << 16);
         }
         const bool resid = (op == OP_O || op == OP_DOWN);
-        for (int c0 = 0; c0 < p.npad; c0 += 16) {
+        for (int c0 = 16 * (wc >> 2); c0 < p.npad; c0 += 32) {
             // the residual stream's values are read before the partial sums,
             // all independent loads, so that one round trip covers them
             float xo[16];
@@ -1806,16 +1828,20 @@ struct Consumer {
                 // only this warp's slot: every slot of the step is released
                 // together after the barrier below, so no warp runs a lap ahead
                 const uint32_t sbw = smem_u32(c.ring + (size_t)wait_slot_at(c, consumed + (uint32_t)wsl) * slot_bytes);
-                float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+                // even and odd column slices accumulate separately: two
+                // independent chains of dependent MMAs instead of one
+                float sacc[4] = {0.f, 0.f, 0.f, 0.f}, sodd[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     if (ks < nks) {
                         uint32_t a[4], qf[2];
                         ldsm_x4(a, sbw + kof[ks]);
                         ldsm_x2(qf, qlane + (uint32_t)(ks * 32));
-                        mma_bf16_16816(sacc, a, qf);
+                        mma_bf16_16816((ks & 1) ? sodd : sacc, a, qf);
                     }
                 }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) sacc[i] += sodd[i];
                 // scores of (token row, head) in the head lanes; -inf past the context
                 float sv[4];
 #pragma unroll
@@ -2404,6 +2430,27 @@ struct Consumer {
     }
 };
 
+// Wait (bounded) until the scheduler has released queue position i; false
+// on the scheduler's abort mark, a local abort or a timeout (recorded).
+__device__ bool wait_ready(const Ctx &c, int i) {
+    uint32_t r = ld_acquire_cta(&c.sc->ready);
+    if (r == kReadyAbort) return false;
+    if (r >= (uint32_t)(i + 1)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        r = ld_acquire_cta(&c.sc->ready);
+        if (r == kReadyAbort) return false;
+        if (r >= (uint32_t)(i + 1)) return true;
+        if ((it & 63u) == 0) {
+            if (local_abort(c)) return false;
+            if (globaltimer_ns() - t0 > 4 * c.p->timeout_ns) {
+                record_error(c, 4, SITE_READY_WAIT, i);
+                return false;
+            }
+        }
+    }
+}
+
 template <bool JIT>
 __device__ void compute_role(const Ctx &c, const Task *q, int nt) {
     const KParams &p = *c.p;
@@ -2430,20 +2477,7 @@ __device__ void compute_role(const Ctx &c, const Task *q, int nt) {
             t = q[i];
         }
         if (!task_active(p, t)) continue;
-        // wait for the scheduler to release task i
-        if (ld_acquire_cta(&c.sc->ready) < (uint32_t)(i + 1)) {
-            uint64_t t0 = globaltimer_ns();
-            for (uint32_t it = 1;; ++it) {
-                if (ld_acquire_cta(&c.sc->ready) >= (uint32_t)(i + 1)) break;
-                if ((it & 63u) == 0) {
-                    if (local_abort(c)) break;
-                    if (globaltimer_ns() - t0 > 4 * p.timeout_ns) {
-                        record_error(c, 4, SITE_READY_WAIT, i);
-                        break;
-                    }
-                }
-            }
-        }
+        wait_ready(c, i);  // the scheduler releases task i (an abort is seen at the barrier below)
         if (compute_bar_or(local_abort(c))) return;  // every compute warp takes the same branch
         uint64_t *tr = cs.tracing ? trace_slot(p, i) : nullptr;
         if (tr) tr[1] = globaltimer_ns();
@@ -2457,9 +2491,11 @@ __device__ void compute_role(const Ctx &c, const Task *q, int nt) {
         const bool aborted = compute_bar_or(local_abort(c));  // every output row of the task is written
         if (tr) {
             tr[2] = globaltimer_ns();
-            tr[3] = cs.full_wait_ns;
-            tr[6] = cs.act_wait_ns;
-            tr[7] = cs.acc_wait_ns;
+            if (!(p.tc && is_proj(t.op))) {  // a projection's waits are the MMA warp's
+                tr[3] = cs.full_wait_ns;
+                tr[6] = cs.act_wait_ns;
+                tr[7] = cs.acc_wait_ns;
+            }
             cs.full_wait_ns = cs.act_wait_ns = cs.acc_wait_ns = 0;
         }
         if (aborted) return;
@@ -2472,6 +2508,47 @@ __device__ void compute_role(const Ctx &c, const Task *q, int nt) {
 
 // JIT: dynamic dispatch (tasks claimed at run time); otherwise every CTA
 // walks its static queue.
+// ------------------------------------------------------------- MMA warp
+// Batched path: one thread walks the same task sequence as the compute warps
+// and issues every projection's tcgen05 MMAs; for an attention task it only
+// counts the ring slots the compute warps consume, so that its slot and
+// phase arithmetic stays in step with theirs.  A projection waits for its
+// release by the scheduler first: its dependencies include this CTA's
+// earlier tasks, so by then every slot counted for them has been consumed
+// and the ring's phases (one parity bit per slot) are the ones counted.
+// Without that wait the warp would reach a weight slot's barrier laps ahead
+// of the attention tasks still cycling the ring.
+template <bool JIT>
+__device__ void mma_role(const Ctx &c, const Task *q, int nt) {
+    const KParams &p = *c.p;
+    if (!p.tc || (threadIdx.x & 31) != 0) return;
+    Consumer ms;
+    ms.ns = (uint32_t)p.num_slots;
+    ms.slot_bytes = (uint32_t)p.slot_bytes;
+    ms.tcm = true;
+    ms.ct = -1;
+    ms.wc = -1;
+    ms.lane = 0;
+    ms.tracing = p.trace != nullptr && !JIT;
+    for (int i = 0;; ++i) {
+        Task t;
+        if (JIT) {
+            if (!jit_task(c, i, &t, &c.sc->jmma)) break;
+        } else {
+            if (i >= nt) break;
+            t = q[i];
+        }
+        if (!task_active(p, t)) continue;
+        if (is_proj(t.op)) {
+            if (!wait_ready(c, i)) break;
+            if (!ms.mma_task(c, t, ms.tracing ? trace_slot(p, i) : nullptr)) break;
+        } else if (t.op == OP_ATTN) {
+            const AttnRange r = attn_range(p, t);
+            if (r.blo < r.bhi) ms.consumed += (uint32_t)((r.bhi - r.blo) * (kAttnBlock / p.attn_ts));
+        }
+    }
+}
+
 template <bool JIT>
 __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant__ KParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -2482,7 +2559,7 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant_
     const Task *q = JIT ? p.tasks : p.tasks + p.queue_off[blockIdx.x];
     const int nt = JIT ? 0 : p.queue_off[blockIdx.x + 1] - p.queue_off[blockIdx.x];
     const int warp = threadIdx.x >> 5;
-    constexpr int kWarpMma = 2;  // batched path: TMEM owner and MMA issuer (compute warp 0)
+    constexpr int kWarpMma = 2 + kComputeWarps;  // batched path: TMEM owner and MMA issuer (the last warp)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.num_slots; ++s) {
@@ -2503,7 +2580,7 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant_
         sc->ready = 0;
         sc->abort = global_abort(p) ? 1u : 0u;  // a recorded error stays sticky
         sc->last_flag = 0;
-        sc->jclaimed = sc->jdone = sc->jprod = sc->jcomp = 0;
+        sc->jclaimed = sc->jdone = sc->jprod = sc->jcomp = sc->jmma = 0;
         fence_mbar_init();
     }
     if (p.tc && warp == kWarpMma) {
@@ -2539,6 +2616,7 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant_
     if (!local_abort(c)) {
         if (warp == kWarpSched) scheduler_role<JIT>(c, q, nt);
         else if (warp == kWarpProd) producer_role<JIT>(c, q, nt);
+        else if (warp == kWarpMma) mma_role<JIT>(c, q, nt);
         else compute_role<JIT>(c, q, nt);
     }
     if (p.tc && threadIdx.x == kWarpMma * 32) {

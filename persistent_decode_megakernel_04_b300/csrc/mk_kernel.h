@@ -13,7 +13,7 @@ constexpr int kComputeWarps = 8;
 constexpr int kComputeThreads = kComputeWarps * 32;
 constexpr int kWarpSched = 0;
 constexpr int kWarpProd = 1;
-constexpr int kThreads = (2 + kComputeWarps) * 32;  // 320
+constexpr int kThreads = (3 + kComputeWarps) * 32;  // 352: scheduler, producer, 8 compute warps, MMA warp
 constexpr int kMaxSlots = 16;
 constexpr int kMaxGroup = 8;      // q heads per kv head
 constexpr int kMaxHeadDim = 128;
