@@ -129,7 +129,11 @@ typedef struct {
                               at run time, batch-1 projections cut into n ranges per CTA (at most
                               16; the tensor-core path keeps one range per CTA).  Not with trace;
                               the ablation build needs static dispatch */
-    int32_t reserved[2];
+    int32_t test_poison_scratch; /* testing: nonzero fills every activation buffer of the plan's
+                                    scratch with 0xFF bytes (NaN as fp32 and as bf16) before each
+                                    step, so that a value a step reads without having written it
+                                    shows up as NaN in the logits; costs a memset per buffer */
+    int32_t reserved[1];
 } mk_plan_options;
 
 typedef struct mk_plan mk_plan; /* opaque, library-owned */

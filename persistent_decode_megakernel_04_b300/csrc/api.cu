@@ -19,6 +19,9 @@ using namespace mk;
 struct mk_plan {
     mk_model_cfg cfg;
     mk_plan_options opt;
+    // test_poison_scratch: the (address, bytes) ranges of activation scratch
+    // filled with 0xFF (NaN as fp32 and as bf16) before every step
+    std::vector<std::pair<void *, size_t>> poison;
     PlanTables tables;
     int device = 0;
     int variant = 0;
@@ -238,11 +241,19 @@ mk_status clear_trace(mk_plan *p, cudaStream_t s) {
         cudaMemsetAsync(p->d_trace, 0, (size_t)p->tables.g.num_ctas * p->trace_stride * 8 * sizeof(uint64_t), s));
 }
 
+// test_poison_scratch: NaN-fill the activation scratch before a step.
+mk_status poison_scratch(mk_plan *p, cudaStream_t s) {
+    for (const auto &r : p->poison)
+        if (cudaMemsetAsync(r.first, 0xFF, r.second, s) != cudaSuccess) return cuda_status(cudaGetLastError());
+    return MK_OK;
+}
+
 mk_status launch_step(mk_plan *p, const KParams &k, cudaStream_t s) {
     cudaError_t e = cudaSetDevice(p->device);
     if (e != cudaSuccess) return cuda_status(e);
     mk_status st = clear_trace(p, s);
     if (st != MK_OK) return st;
+    if ((st = poison_scratch(p, s)) != MK_OK) return st;
     return cuda_status(launch_megakernel(k, p->variant, p->tables.g.num_ctas, p->smem, true, s));
 }
 
@@ -500,6 +511,29 @@ mk_status mk_plan_create_ex(const mk_model_cfg *cfg, const mk_weight_ptrs *w, co
     }
     if (e == cudaSuccess) e = cudaMemset(p->d_ctl, 0, (size_t)p->cl.total * sizeof(uint32_t));
     if (e == cudaSuccess) e = launch_rope_table(p->d_rope, c.max_seq, c.head_dim, c.rope_theta, 0);
+    if (p->opt.test_poison_scratch) {
+        // every buffer a step writes before it reads; the split-bf16 operands
+        // only in their batch rows (high and low parts), the padding rows
+        // must stay zero
+        const size_t B = (size_t)c.batch;
+        auto add = [&](void *q, size_t bytes) { p->poison.emplace_back(q, bytes); };
+        add(p->d_x, B * c.hidden * 4);
+        add(p->d_qkv, B * qkv_rows * 4);
+        add(p->d_part, n_part * 4);
+        add(p->d_attn, B * c.n_q_heads * c.head_dim * 4);
+        add(p->d_h, B * c.ffn_dim * 4);
+        if (g.tc) {
+            const size_t qd = (size_t)c.n_q_heads * c.head_dim;
+            const size_t widths[3] = {(size_t)c.hidden, qd, (size_t)c.ffn_dim};
+            uint16_t *bufs[3] = {p->d_xa, p->d_attn_a, p->d_h_a};
+            for (int i = 0; i < 3; ++i) {
+                add(bufs[i], B * widths[i] * 2);
+                add(bufs[i] + (size_t)g.npad * widths[i], B * widths[i] * 2);
+            }
+            add(p->d_ssq, B * g.h_tiles * 4);
+            add(p->d_tc_part, (size_t)g.num_ctas * 2 * 2 * g.npad * kTcTileM * 4);
+        }
+    }
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -612,6 +646,7 @@ mk_status mk_decode_step_ablation(mk_plan *p, const int32_t *tokens, const int32
     if (cudaSetDevice(p->device) != cudaSuccess) return cuda_status(cudaGetLastError());
     KParams k = step_params(p, tokens, 1, positions, 1, kv, logits);
     if ((st = clear_trace(p, s)) != MK_OK) return st;
+    if ((st = poison_scratch(p, s)) != MK_OK) return st;  // once per step: later launches read earlier ones
     static const int kOps[] = {OP_QKV, OP_ATTN, OP_O, OP_GU, OP_DOWN};
     if (p->tables.g.tc) {
         k.only_op = OP_EMBED;
@@ -652,6 +687,7 @@ mk_status ensure_prefill_engine(mk_plan *p) {
     o.timeout_ms = p->opt.timeout_ms;
     o.tensor_cores = 1;
     o.kv_append = 1;
+    o.test_poison_scratch = p->opt.test_poison_scratch;
     const int L = c.n_layers;
     std::vector<const void *> f[9];
     for (auto &v : f) v.resize(L);

@@ -460,3 +460,23 @@ def test_long_splits_warp_local_attention(cuda_device, m, batch):
     else:
         harness.run_teacher_forced_batch(plan, kv, model, prompts(batch, 300, seed=11, vocab=m.vocab), 3, max_seq,
                                          rows=[0, batch - 1])
+
+
+@pytest.mark.parametrize("case", [dict(batch=1), dict(batch=1, prefill_by_decode=1), dict(batch=1, tensor_cores=1),
+                                  dict(batch=24), dict(batch=6, jit=1)],
+                         ids=["b1", "b1-decode-prefill", "b1-tc", "b24", "b6-jit"])
+def test_poisoned_scratch_is_never_read_unwritten(cuda_device, case):
+    """Every activation buffer of the plan's scratch is NaN-filled before each
+    step (test_poison_scratch): the prompt prefill (chunked engine, or decode
+    steps), teacher-forced decode steps and launch-per-operator steps must
+    still match the oracle, so no step reads a scratch value it did not write
+    in that step."""
+    m = TINY
+    B = case.pop("batch")
+    max_seq = 128
+    plan, kv = harness.gpu_plan(m, max_seq, batch=B, opts=mk.mk_plan_options(test_poison_scratch=1, **case))
+    model = harness.oracle_model(m)
+    prompts = np.stack([synth.tokens(21, 4, 400 + b, m.vocab) for b in range(B)])
+    rows = sorted({0, B - 1})
+    harness.run_teacher_forced_batch(plan, kv, model, prompts, 4, max_seq, rows=rows,
+                                     ablation_every=0 if case.get("jit") else 3)
