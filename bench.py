@@ -469,28 +469,41 @@ def run_mk(args, wl):
     peak, peak_src = measured_peak()
     clk = clocks.summary()
 
-    # end to end through the host-buffer entry point: token in, logits out, host argmax
+    # end to end through the host-buffer entry points, from pinned host
+    # memory: (1) the greedy step (tokens and positions in, the picked tokens
+    # out; the pick runs in the launch), the `e2e` figure; (2) tokens in,
+    # logits out, the argmax on the host, reported beside it
     h_tok = torch.empty(B, dtype=torch.int32).pin_memory()
     h_pos = torch.empty(B, dtype=torch.int32).pin_memory()
+    h_nxt = torch.empty(B, dtype=torch.int32).pin_memory()
     h_log = torch.empty((B, m.vocab), dtype=torch.float32).pin_memory()
     h_tok.copy_(tok.cpu())
     h_pos.copy_(pos.cpu())
-    n_tok, n_pos, n_log = h_tok.numpy(), h_pos.numpy(), h_log.numpy()
+    n_tok, n_pos, n_nxt, n_log = h_tok.numpy(), h_pos.numpy(), h_nxt.numpy(), h_log.numpy()
 
-    def e2e_step():
+    def e2e_greedy():
+        plan.decode_step_greedy_host(h_tok, h_pos, kv, h_nxt)
+        n_tok[:] = n_nxt
+        n_pos[:] += 1
+
+    def e2e_logits():
         plan.decode_step_host(h_tok, h_pos, kv, h_log)
         n_tok[:] = np.argmax(n_log, axis=1)
         n_pos[:] += 1
 
-    for _ in range(args.warmup):  # first-call costs stay out of the timed region, as for `value`
-        e2e_step()
-    # the same context lengths as the device-timed steps (their cache slots are rewritten)
-    n_pos[:] = ctx0 - 1
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(args.e2e_steps):
-        e2e_step()
-    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.e2e_steps
+    def time_e2e(step_fn):
+        for _ in range(args.warmup):  # first-call costs stay out of the timed region, as for `value`
+            step_fn()
+        # the same context lengths as the device-timed steps (their cache slots are rewritten)
+        n_pos[:] = ctx0 - 1
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            step_fn()
+        return (time.perf_counter() - t0) * 1e3 / args.e2e_steps
+
+    e2e_ms = time_e2e(e2e_greedy)
+    e2e_logits_ms = time_e2e(e2e_logits)
 
     # launch-per-operator ablation of the same task code
     abl = {}
@@ -566,7 +579,10 @@ def run_mk(args, wl):
                          "bytes_per_step_mean": bytes_total / args.steps},
             "clocks": clk,
             "e2e": {"value": e2e_ms / B, "unit": "ms/token", "h2d_bytes_per_step": 8 * B,
-                    "d2h_bytes_per_step": 4 * B * m.vocab},
+                    "d2h_bytes_per_step": 4 * B, "api": "mk_decode_step_greedy_host",
+                    "logits_to_host": {"value": e2e_logits_ms / B, "unit": "ms/token", "h2d_bytes_per_step": 8 * B,
+                                       "d2h_bytes_per_step": 4 * B * m.vocab,
+                                       "api": "mk_decode_step_host + host argmax"}},
             "gpu_launches": (1 if fused else 2) * args.steps,
             "ablation": abl,
             "prefill": prefill_info,

@@ -227,13 +227,26 @@ mk_status mk_greedy_next(mk_plan *plan, const float *logits, int32_t *tokens, in
  * the argmax of row b of logits (the lowest index among equal maxima; NaN
  * never wins, and a row without a finite maximum gives 0x7FFFFFFF) and
  * positions[b] is incremented, exactly as mk_decode_step then
- * mk_greedy_next.  At batch 1 the pick runs inside the decode launch (each
+ * mk_greedy_next.  The pick runs inside the decode launch: at batch 1 (each
  * CTA's maximum over its LM-head rows, merged with one 64-bit atomic max);
- * batched plans launch the pick after the step.  tokens and positions are
+ * batched plans pick in the tensor-core LM-head epilogue (each tile's best
+ * row per sequence, one 64-bit atomic max per sequence and CTA), and the last
+ * CTA out writes the tokens.  tokens and positions are
  * device arrays [batch], read by the step and rewritten after it; logits are
  * still written.  Errors as mk_decode_step. */
 mk_status mk_decode_step_greedy(mk_plan *plan, int32_t *tokens, int32_t *positions, const mk_kv_cache *kv,
                                 float *logits, void *stream);
+
+/* Passage: token-by-token greedy generation ("Compilar LLM en un
+ * MegaKernel…", "Valor central de MPK"), driven from host memory.
+ * mk_decode_step_greedy with HOST buffers: copies tokens and positions (host
+ * int32 [batch]) in, runs the step with the pick inside the launch, copies
+ * the picked tokens (host int32 [batch]) out and synchronises `stream`.  The
+ * logits stay in plan-owned device memory; positions_host is not changed
+ * (the next step passes positions + 1).  Returns device errors of this step
+ * directly. */
+mk_status mk_decode_step_greedy_host(mk_plan *plan, const int32_t *tokens_host, const int32_t *positions_host,
+                                     const mk_kv_cache *kv, int32_t *next_tokens_host, void *stream);
 
 /* Passage: the 1-2 us task-switch cost that "Compilar LLM en un
  * MegaKernel…" reports ("Método de ejecución basado en eventos"); this call

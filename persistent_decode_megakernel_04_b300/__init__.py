@@ -58,7 +58,7 @@ class mk_task_info(ctypes.Structure):
 
 _lib = None
 EXPORTS = ("mk_plan_create", "mk_plan_create_ex", "mk_decode_step", "mk_decode_step_ablation",
-           "mk_decode_step_host", "mk_prefill", "mk_prefill_row", "mk_greedy_next", "mk_plan_last_error",
+           "mk_decode_step_host", "mk_decode_step_greedy_host", "mk_prefill", "mk_prefill_row", "mk_greedy_next", "mk_plan_last_error",
            "mk_status_string", "mk_error_site_string", "mk_plan_destroy", "mk_plan_describe", "mk_plan_trace",
            "mk_decode_step_noalloc", "mk_decode_step_greedy", "mk_pages_create", "mk_pages_admit",
            "mk_pages_extend", "mk_pages_retire", "mk_pages_free_count", "mk_pages_scratch_page", "mk_pages_table",
@@ -79,6 +79,7 @@ def lib():
         L.mk_decode_step_ablation.argtypes = step
         L.mk_decode_step_greedy.argtypes = step
         L.mk_decode_step_host.argtypes = step
+        L.mk_decode_step_greedy_host.argtypes = step
         L.mk_prefill.argtypes = [_vp, _vp, _i32, P(mk_kv_cache), _vp, _vp]
         L.mk_greedy_next.argtypes = [_vp, _vp, _vp, _vp, _vp]
         L.mk_plan_last_error.argtypes = [_vp, _vp, P(mk_device_error)]
@@ -283,6 +284,13 @@ class Plan:
         st = lib().mk_decode_step_host(self.h, ptr(tokens_host), ptr(positions_host), ctypes.byref(kv.desc),
                                        ptr(logits_host), _stream_ptr(stream))
         _check(st, "mk_decode_step_host")
+
+    def decode_step_greedy_host(self, tokens_host, positions_host, kv: KVCache, next_tokens_host, stream=None):
+        """Host int32 buffers: tokens and positions in, the step's greedy picks out; synchronises."""
+        ptr = lambda a: a.ctypes.data if hasattr(a, "ctypes") else a.data_ptr()
+        st = lib().mk_decode_step_greedy_host(self.h, ptr(tokens_host), ptr(positions_host), ctypes.byref(kv.desc),
+                                              ptr(next_tokens_host), _stream_ptr(stream))
+        _check(st, "mk_decode_step_greedy_host")
 
     def prefill(self, tokens, kv: KVCache, last_logits, stream=None):
         T = tokens.shape[-1]

@@ -824,6 +824,26 @@ mk_status mk_decode_step_host(mk_plan *p, const int32_t *tokens_host, const int3
     return mk_plan_last_error(p, stream, nullptr);
 }
 
+mk_status mk_decode_step_greedy_host(mk_plan *p, const int32_t *tokens_host, const int32_t *positions_host,
+                                     const mk_kv_cache *kv, int32_t *next_tokens_host, void *stream) {
+    if (!p || !tokens_host || !positions_host || !next_tokens_host) return MK_ERR_INVALID;
+    mk_status st = check_kv(p, kv);
+    if (st != MK_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t nb = (size_t)p->cfg.batch * sizeof(int32_t);
+    cudaError_t e = cudaMemcpyAsync(p->d_stage_tok, tokens_host, nb, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(p->d_stage_pos, positions_host, nb, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_status(e);
+    KParams k = step_params(p, p->d_stage_tok, 1, p->d_stage_pos, 1, kv, p->d_stage_logits);
+    k.greedy = 1;  // the step rewrites the staged tokens (and positions) with its pick
+    k.next_tokens = p->d_stage_tok;
+    k.next_positions = p->d_stage_pos;
+    if ((st = launch_step(p, k, s)) != MK_OK) return st;
+    e = cudaMemcpyAsync(next_tokens_host, p->d_stage_tok, nb, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_status(e);
+    return mk_plan_last_error(p, stream, nullptr);
+}
+
 mk_status mk_plan_trace(mk_plan *p, void *stream, uint64_t *out, int64_t capacity, int32_t *num_ctas,
                         int32_t *max_tasks) {
     if (!p || !p->d_trace) return MK_ERR_INVALID;

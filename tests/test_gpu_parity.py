@@ -348,6 +348,20 @@ def test_fused_greedy_step_matches_step_then_pick(cuda_device, name, batch):
         assert torch.equal(logits_a, logits_b), f"step {step}: logits differ"
         assert torch.equal(tok_a, tok_b) and torch.equal(pos_a, pos_b), f"step {step}: {tok_a} {tok_b} {pos_a} {pos_b}"
         assert int(pos_b[0]) == 41 + step
+    # the host-buffer form from the same state: its picks are the device form's
+    kv_b.k.copy_(kv_a.k)
+    kv_b.v.copy_(kv_a.v)
+    h_tok = tok_a.cpu().numpy().copy()
+    h_pos = pos_a.cpu().numpy().copy()
+    h_nxt = np.zeros(batch, np.int32)
+    for step in range(3):
+        plan.decode_step_greedy(tok_a, pos_a, kv_a, logits_a)
+        plan.decode_step_greedy_host(h_tok, h_pos, kv_b, h_nxt)
+        plan.check()
+        assert np.array_equal(h_nxt, tok_a.cpu().numpy()), f"host step {step}: {h_nxt} {tok_a}"
+        h_tok[:] = h_nxt
+        h_pos += 1
+        assert np.array_equal(h_pos, pos_a.cpu().numpy())
 
 
 @pytest.mark.parametrize("batch", [1, 8])
