@@ -359,24 +359,33 @@ __device__ __forceinline__ int64_t kv_offset(const KParams &p, int layer, int32_
 
 struct Producer {
     uint32_t issued = 0;
+    // slot index and phase bit of ring slot number `issued`, advanced with it
+    // (one single-thread loop: no division per slot)
+    uint32_t si = 0, sph = 0;
     uint64_t pol;
     uint64_t *tr = nullptr;  // trace entry of the current task
     uint32_t ns = 0;         // ring slots (kept in a register)
     uint32_t slot_bytes = 0;
     uint32_t fmax = 0;       // copies in flight at most (0: every free slot)
 
+    // Every call is followed by exactly one ++issued once the slot's copies
+    // are issued; si and sph move on here.
     __device__ bool acquire_slot(const Ctx &c, uint32_t *slot) {
-        const uint32_t s = issued % ns;
-        const uint32_t round = issued / ns;
+        const uint32_t s = si;
         const uint64_t t0 = tr ? globaltimer_ns() : 0;
-        if (!wait_mbar(c, &c.sc->empty[s], (round & 1u) ^ 1u, SITE_EMPTY_WAIT)) return false;
+        if (!wait_mbar(c, &c.sc->empty[s], sph ^ 1u, SITE_EMPTY_WAIT)) return false;
         if (fmax != 0 && issued >= fmax) {
             // copy number issued - fmax must have landed: fewer bytes queued
             // in the memory system ahead of this SM's other requests, and a
             // gpu-scope fence (which waits for this SM's copies in flight)
-            // stays short
-            const uint32_t k = issued - fmax;
-            if (!wait_mbar(c, &c.sc->full[k % ns], (k / ns) & 1u, SITE_EMPTY_WAIT)) return false;
+            // stays short.  fmax < ns: that copy is in this round or the last.
+            const uint32_t ks = (s >= fmax) ? s - fmax : s + ns - fmax;
+            const uint32_t kph = (s >= fmax) ? sph : (sph ^ 1u);
+            if (!wait_mbar(c, &c.sc->full[ks], kph, SITE_EMPTY_WAIT)) return false;
+        }
+        if (++si == ns) {
+            si = 0;
+            sph ^= 1u;
         }
         if (tr) {
             const uint64_t t1 = globaltimer_ns();
@@ -683,6 +692,7 @@ __device__ void producer_role(const Ctx &c, const Task *q, int nt) {
 // earlier in this launch by other CTAs) into the activation ring.
 struct ActProducer {
     uint32_t issued = 0;
+    uint32_t si = 0, sph = 0;  // slot index and phase bit of activation slot number `issued`
     uint64_t pol;
 
     __device__ bool run(const Ctx &c, const Task &t) {
@@ -691,12 +701,18 @@ struct ActProducer {
         const void *map = tmap(p, act_map(p, t.op));
         const uint32_t ns = (uint32_t)p.num_aslots;
         fence_proxy_async_global();  // generic-proxy writes (ordered by the acquire) -> TMA reads
+        int32_t kc = t.a0 % g.kchunks;
         for (int32_t u = t.a0; u < t.a1; ++u) {
-            const uint32_t s = issued % ns, round = issued / ns;
-            if (!wait_mbar(c, &c.sc->aempty[s], (round & 1u) ^ 1u, SITE_EMPTY_WAIT)) return false;
+            const uint32_t s = si;
+            if (!wait_mbar(c, &c.sc->aempty[s], sph ^ 1u, SITE_EMPTY_WAIT)) return false;
             mbar_arrive_expect_tx(&c.sc->afull[s], (uint32_t)p.aslot_bytes);
-            tma_load_2d(c.aring + (size_t)s * p.aslot_bytes, map, (u % g.kchunks) * kTcTileK, 0, &c.sc->afull[s], pol);
+            tma_load_2d(c.aring + (size_t)s * p.aslot_bytes, map, kc * kTcTileK, 0, &c.sc->afull[s], pol);
             ++issued;
+            if (++si == ns) {
+                si = 0;
+                sph ^= 1u;
+            }
+            if (++kc == g.kchunks) kc = 0;
         }
         return true;
     }
@@ -1428,10 +1444,19 @@ struct Consumer {
         return ok;
     }
 
+    // One thread.  Slot indices and phase bits advance by increments, and the
+    // operand descriptors are the ring bases' plus the slot offset (the
+    // start-address field is the low 14 bits, address / 16): a unit costs
+    // its waits, four or eight MMAs and the commits, no division.
     __device__ bool mma_issuer(const Ctx &c, const Task &t, const TcGeom &g, int mats, int32_t t0, int32_t t1) {
         const KParams &p = *c.p;
         SmemCtl *sc = c.sc;
         const uint32_t nas = (uint32_t)p.num_aslots;
+        uint32_t wi = consumed % ns, wph = (consumed / ns) & 1u;
+        uint32_t ai = aconsumed % nas, aph = (aconsumed / nas) & 1u;
+        const uint64_t wdesc0 = umma_desc_sw128(smem_u32(c.ring)), adesc0 = umma_desc_sw128(smem_u32(c.aring));
+        const uint32_t wstep = slot_bytes >> 4, astep = (uint32_t)p.aslot_bytes >> 4;
+        const uint32_t idesc = p.idesc, mstride = 2u * (uint32_t)p.npad;
         uint32_t sg = seg;
         for (int32_t tile = t0; tile <= t1; ++tile, ++sg) {
             const int32_t klo = (tile == t0) ? t.a0 % g.kchunks : 0;
@@ -1441,38 +1466,46 @@ struct Consumer {
             if (!wait_mbar(c, &sc->acc_empty[ab], (use & 1u) ^ 1u, SITE_ACC_WAIT)) return false;
             if (tracing) acc_wait_ns += globaltimer_ns() - t0;
             tc_fence_after();
-            const uint32_t dcol = sc->tmem_base + ab * 4u * (uint32_t)p.npad;
+            const uint32_t dcol = sc->tmem_base + ab * 2u * mstride;
             for (int32_t k = klo; k < khi; ++k) {
                 uint32_t ws[2] = {0u, 0u};
                 if (tracing) t0 = globaltimer_ns();
                 for (int m = 0; m < mats; ++m) {
-                    ws[m] = consumed % ns;
-                    if (!wait_mbar(c, &sc->full[ws[m]], (consumed / ns) & 1u, SITE_FULL_WAIT)) return false;
-                    ++consumed;
+                    ws[m] = wi;
+                    if (!wait_mbar(c, &sc->full[wi], wph, SITE_FULL_WAIT)) return false;
+                    if (++wi == ns) {
+                        wi = 0;
+                        wph ^= 1u;
+                    }
                 }
                 if (tracing) {
                     const uint64_t t1 = globaltimer_ns();
                     full_wait_ns += t1 - t0;
                     t0 = t1;
                 }
-                const uint32_t as = aconsumed % nas;
-                if (!wait_mbar(c, &sc->afull[as], (aconsumed / nas) & 1u, SITE_FULL_WAIT)) return false;
-                ++aconsumed;
+                const uint32_t as = ai;
+                if (!wait_mbar(c, &sc->afull[as], aph, SITE_FULL_WAIT)) return false;
+                if (++ai == nas) {
+                    ai = 0;
+                    aph ^= 1u;
+                }
                 if (tracing) act_wait_ns += globaltimer_ns() - t0;
                 tc_fence_after();
-                const uint32_t abase = smem_u32(c.aring + (size_t)as * p.aslot_bytes);
+                const uint64_t ad = adesc0 + (uint64_t)(as * astep);
                 for (int m = 0; m < mats; ++m) {
-                    const uint32_t wbase = smem_u32(c.ring + (size_t)ws[m] * slot_bytes);
+                    const uint64_t wd = wdesc0 + (uint64_t)(ws[m] * wstep);
 #pragma unroll
-                    for (int kk = 0; kk < kTcTileK / 16; ++kk)
-                        umma_bf16(dcol + (uint32_t)(m * 2 * p.npad), umma_desc_sw128(wbase + kk * 32),
-                                  umma_desc_sw128(abase + kk * 32), p.idesc, (k > klo || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < kTcTileK / 16; ++kk)  // K = 16 bf16 = 32 bytes = 2 descriptor units
+                        umma_bf16(dcol + (uint32_t)m * mstride, wd + 2u * kk, ad + 2u * kk, idesc,
+                                  (k > klo || kk > 0) ? 1u : 0u);
                 }
                 for (int m = 0; m < mats; ++m) umma_commit(&sc->empty[ws[m]]);
                 umma_commit(&sc->aempty[as]);
             }
             umma_commit(&sc->acc_full[ab]);
         }
+        consumed += (uint32_t)((t.a1 - t.a0) * mats);
+        aconsumed += (uint32_t)(t.a1 - t.a0);
         return true;
     }
 
