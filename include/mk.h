@@ -133,7 +133,11 @@ typedef struct {
                                     scratch with 0xFF bytes (NaN as fp32 and as bf16) before each
                                     step, so that a value a step reads without having written it
                                     shows up as NaN in the logits; costs a memset per buffer */
-    int32_t reserved[1];
+    int32_t tc_tile_split; /* tensor-core path: at most this many worker CTAs share one 128-row
+                              tile of a projection; small projections then run on fewer CTAs
+                              with fewer partial sums to add (0: every CTA takes a range of
+                              every projection) */
+    int32_t reserved[2];
 } mk_plan_options;
 
 typedef struct mk_plan mk_plan; /* opaque, library-owned */

@@ -174,8 +174,8 @@ __device__ __forceinline__ int weight_map(const KParams &p, int op, int layer, i
     }
 }
 
-// Which range (0 .. num_ctas-1) owns unit u when `units` units are cut into
-// num_ctas balanced contiguous ranges [c*U/N, (c+1)*U/N).
+// Which range (0 .. n-1) owns unit u when `units` units are cut into n
+// balanced contiguous ranges [c*U/n, (c+1)*U/n).
 __device__ __forceinline__ int32_t range_of(int64_t u, int64_t units, int64_t n) {
     return (int32_t)(((u + 1) * n - 1) / units);
 }
@@ -1529,7 +1529,7 @@ struct Consumer {
             }
         }
         epi_bar();
-        const int64_t U = g.units, NR = p.num_ctas;
+        const int64_t U = g.units, NR = g.nranges;
         const int32_t rc = t.a2;  // this task's range number
         uint32_t sg = seg;
         for (int32_t tile = t0; tile <= t1; ++tile, ++sg) {
@@ -1590,7 +1590,7 @@ struct Consumer {
     // Partial-sum slot [2][npad][128] of range rc for row tile `tile`: slot 0
     // when the tile is the range's first, else slot 1 (its last).
     __device__ static float *part_ptr(const KParams &p, int32_t rc, int32_t tile, const TcGeom &g) {
-        const int64_t first_tile = range_start(rc, g.units, p.num_ctas) / g.kchunks;
+        const int64_t first_tile = range_start(rc, g.units, g.nranges) / g.kchunks;
         const int sidx = (first_tile == tile) ? 0 : 1;
         return p.part + ((size_t)rc * 2 + sidx) * 2 * (size_t)p.npad * kTcTileM;
     }
@@ -1658,7 +1658,7 @@ struct Consumer {
                             const int32_t cc = cg + j;
                             if (cc == rc) {
                                 tmem_ld_split16(tq + (uint32_t)(m * 2 * p.npad + c0), p.npad, w[j]);
-                            } else if (cc <= cl && range_nonempty(cc, g.units, p.num_ctas)) {
+                            } else if (cc <= cl && range_nonempty(cc, g.units, g.nranges)) {
                                 const float *src = part_ptr(p, cc, tile, g) + ((size_t)m * p.npad + c0) * kTcTileM + r;
 #pragma unroll
                                 for (int i = 0; i < 16; ++i) w[j][i] = __ldcg(src + (size_t)i * kTcTileM);

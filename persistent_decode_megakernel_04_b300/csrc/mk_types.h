@@ -74,6 +74,7 @@ struct TcGeom {
     int32_t tiles, kchunks, units;
     int32_t tiles_q, tiles_k;  // QKV only
     int32_t ctr_off;           // first row-tile counter of this operator
+    int32_t nranges;           // contiguous balanced ranges the units are cut into (one per task)
 };
 
 // Device error-word sites.

@@ -168,6 +168,13 @@ mk_status build_plan(const mk_model_cfg &cfg, const mk_plan_options &opt, PlanTa
         ctr += g.tcg[OP_DOWN].tiles;
         g.tcg[OP_LM] = make_tc_geom(H, V, ctr);
         ctr += g.tcg[OP_LM].tiles;
+        // ranges per projection: every CTA, or at most tc_tile_split per row tile
+        for (int op : {OP_QKV, OP_O, OP_GU, OP_DOWN, OP_LM}) {
+            TcGeom &t = g.tcg[op];
+            t.nranges = opt.num_ctas;
+            if (opt.tc_tile_split > 0)
+                t.nranges = (int32_t)std::min<int64_t>(opt.num_ctas, (int64_t)t.tiles * opt.tc_tile_split);
+        }
         g.n_tile_ctrs = ctr;
     }
 
@@ -200,14 +207,25 @@ mk_status build_plan(const mk_model_cfg &cfg, const mk_plan_options &opt, PlanTa
         if (jit) flat.push_back(t);
         else q[perm[c % N]].push_back(t);
     };
-    // Cuts `total` items into R contiguous ranges (balanced to one item);
-    // static dispatch gives range c to CTA perm[c].  Returns the number of tasks.
+    // Ranges of a stage: R, or the tensor-core projection's own count.
+    auto ranges_of = [&](int32_t op) -> int32_t {
+        return (tc && op != OP_EMBED && op != OP_KVA && g.tcg[op].nranges > 0) ? g.tcg[op].nranges : R;
+    };
+    // CTA after the last one the previous stage used: a stage that uses fewer
+    // than every CTA starts there, so that small stages fall on the CTAs the
+    // stage before left idle (or lightly loaded).
+    int32_t cursor = 0;
+    // Cuts `total` items into the stage's ranges (balanced to one item);
+    // static dispatch gives range c to CTA perm[c] (perm[(cursor + c) % N]
+    // for a stage of fewer than N ranges).  Returns the number of tasks.
     auto emit_ranges = [&](int32_t op, int32_t layer, int32_t total, uint16_t wait_ev, uint32_t wait_cnt,
                            uint16_t sig_ev) -> uint32_t {
         uint32_t n = 0;
+        const int32_t Rop = ranges_of(op);
+        const int32_t start = (Rop < N) ? cursor : 0;
         begin_stage();
-        for (int32_t c = 0; c < R; ++c) {
-            int32_t r0 = (int32_t)((int64_t)c * total / R), r1 = (int32_t)((int64_t)(c + 1) * total / R);
+        for (int32_t c = 0; c < Rop; ++c) {
+            int32_t r0 = (int32_t)((int64_t)c * total / Rop), r1 = (int32_t)((int64_t)(c + 1) * total / Rop);
             if (r1 <= r0) continue;
             Task t{};
             t.op = (uint8_t)op;
@@ -218,12 +236,13 @@ mk_status build_plan(const mk_model_cfg &cfg, const mk_plan_options &opt, PlanTa
             t.a0 = r0;
             t.a1 = r1;
             t.a2 = c;
-            push(t, c);
+            push(t, start + c);
             ++n;
         }
+        cursor = (int32_t)((start + n) % N);
         return n;
     };
-    auto count_ranges = [&](int32_t total) { return (uint32_t)std::min<int64_t>(total, R); };
+    auto count_ranges = [&](int32_t op, int32_t total) { return (uint32_t)std::min<int64_t>(total, ranges_of(op)); };
 
     uint16_t x_ready_ev = kNoEvent;
     uint32_t x_ready_cnt = 0;
@@ -233,8 +252,8 @@ mk_status build_plan(const mk_model_cfg &cfg, const mk_plan_options &opt, PlanTa
         x_ready_cnt = emit_ranges(OP_EMBED, 0, B * g.h_tiles, kNoEvent, 0, ev);
         x_ready_ev = ev;
     }
-    const uint32_t n_qkv = count_ranges(items(OP_QKV)), n_o = count_ranges(items(OP_O)),
-                   n_gu = count_ranges(items(OP_GU)), n_down = count_ranges(items(OP_DOWN));
+    const uint32_t n_qkv = count_ranges(OP_QKV, items(OP_QKV)), n_o = count_ranges(OP_O, items(OP_O)),
+                   n_gu = count_ranges(OP_GU, items(OP_GU)), n_down = count_ranges(OP_DOWN, items(OP_DOWN));
     auto ev = [&](int32_t l, int32_t op) { return (uint16_t)ev_id(l, op, per); };
     for (int32_t l = 0; l < L; ++l) {
         uint32_t k = emit_ranges(OP_QKV, l, items(OP_QKV), x_ready_ev, x_ready_cnt, ev(l, OP_QKV));
@@ -265,6 +284,7 @@ mk_status build_plan(const mk_model_cfg &cfg, const mk_plan_options &opt, PlanTa
                     t.a3 = S;
                     push(t, i);
                 }
+        cursor = i % N;
         emit_ranges(OP_O, l, items(OP_O), ev(l, OP_ATTN), (uint32_t)(B * nkv), ev(l, OP_O));
         emit_ranges(OP_GU, l, items(OP_GU), ev(l, OP_O), n_o, ev(l, OP_GU));
         emit_ranges(OP_DOWN, l, items(OP_DOWN), ev(l, OP_GU), n_gu, ev(l, OP_DOWN));

@@ -39,7 +39,9 @@ def test_tiny_batched_random_gains_and_ablation(cuda_device):
 
 @pytest.mark.parametrize("opts", [dict(num_ctas=7, attn_splits=3, planner_seed=5),
                                   dict(num_ctas=148, attn_splits=1, num_slots=3, planner_seed=9),
-                                  dict(num_ctas=1)], ids=["7ctas", "3slots", "1cta"])
+                                  dict(num_ctas=1), dict(tc_tile_split=1), dict(tc_tile_split=2, planner_seed=3),
+                                  dict(tc_tile_split=3, num_ctas=20)],
+                         ids=["7ctas", "3slots", "1cta", "split1", "split2", "split3-20ctas"])
 def test_tiny_batched_schedules(cuda_device, opts):
     # row tiles shared by several ranges (fixup), a permuted CTA assignment,
     # a shallow weight ring and a single worker CTA
@@ -79,8 +81,8 @@ def test_batched_rows_equal_single_sequence_runs(cuda_device):
         harness.compare_logits(got[b], l1.cpu().numpy()[0], f"row {b} vs batch-1 run")
 
 
-@pytest.mark.parametrize("B", [8, 32, 64])
-def test_8b_batched_decode_from_seeded_cache(cuda_device, B):
+@pytest.mark.parametrize("B,split", [(8, 0), (32, 0), (64, 0), (64, 2)], ids=["8", "32", "64", "64-split2"])
+def test_8b_batched_decode_from_seeded_cache(cuda_device, B, split):
     """The 8B-shaped decoder at 4096 cached tokens per sequence (paged,
     shuffled pages), in the launch configuration the bench times; the oracle
     checks rows 0 and B-1."""
@@ -88,7 +90,7 @@ def test_8b_batched_decode_from_seeded_cache(cuda_device, B):
     m = wl.model
     ctx, steps = 4096, 2
     max_seq = ((ctx + steps + 64) // 64) * 64
-    plan, kv = harness.gpu_plan(m, max_seq, batch=B)
+    plan, kv = harness.gpu_plan(m, max_seq, batch=B, opts=mk.mk_plan_options(tc_tile_split=split))
     model = harness.oracle_model(m)
     caches = harness.fill_synthetic_cache(kv, model, m, ctx, B, max_seq, rows=(0, B - 1))
     harness.run_from_cache(plan, kv, model, caches, ctx, steps, synth.tokens(B, wl.seed, 0, m.vocab), batch=B)

@@ -334,3 +334,38 @@ def test_dynamic_dispatch_rejects_tracing():
     cfg = mk.model_cfg(SHAPES["tiny"], 1, 128)
     with pytest.raises(mk.MKError):
         mk.mk_plan_describe(cfg, 148, mk.mk_plan_options(jit=1, trace=1))
+
+
+@pytest.mark.parametrize("split", [1, 2, 3])
+def test_tile_split_bounds_the_ranges_per_row_tile(split):
+    """tc_tile_split: a tensor-core projection is cut into at most
+    tiles * split ranges (all CTAs when that is more), each 128-row tile is
+    shared by at most split ranges, the ranges tile the units exactly, a
+    stage of fewer ranges than CTAs starts on the CTA after the previous
+    stage's last, and the schedule still drains."""
+    m = SHAPES["8b"]
+    N, B = 148, 64
+    cfg = mk.model_cfg(m, B, 4160)
+    tasks, n_events = mk.mk_plan_describe(cfg, N, mk.mk_plan_options(tc_tile_split=split))
+    H, I, V, d = m.hidden, m.ffn_dim, m.vocab, m.head_dim
+    qkv_tiles = (m.n_q_heads * d + 127) // 128 + 2 * ((m.n_kv_heads * d + 127) // 128)
+    geo = {mk.OP_QKV: (qkv_tiles, H // 64), mk.OP_O: (H // 128, m.n_q_heads * d // 64),
+           mk.OP_GU: (I // 128, H // 64), mk.OP_DOWN: (H // 128, I // 64), mk.OP_LM: ((V + 127) // 128, H // 64)}
+    for op, (tiles, kchunks) in geo.items():
+        ts = sorted((t for t in tasks if t.op == op and t.layer == (m.n_layers - 1 if op == mk.OP_LM else 3)),
+                    key=lambda t: t.a0)
+        assert len(ts) == min(N, tiles * split), (op, len(ts))
+        assert ts[0].a0 == 0 and ts[-1].a1 == tiles * kchunks
+        assert all(a.a1 == b.a0 for a, b in zip(ts, ts[1:]))
+        assert sorted(t.a2 for t in ts) == list(range(len(ts)))  # range numbers
+        assert len({t.cta for t in ts}) == len(ts)  # one range per CTA
+        for tile in range(tiles):
+            lo, hi = tile * kchunks, (tile + 1) * kchunks
+            assert sum(1 for t in ts if t.a0 < hi and t.a1 > lo) <= max(split, -(-len(ts) // tiles) + 1)
+    # the O projection of a layer starts on the CTA after the attention tasks' last
+    n_att = sum(1 for t in tasks if t.op == mk.OP_ATTN and t.layer == 3)
+    o = [t for t in tasks if t.op == mk.OP_O and t.layer == 3]
+    if len(o) < N:
+        assert min(o, key=lambda t: t.a2).cta == n_att % N
+    ok, _, _ = simulate(m, tasks, n_events)
+    assert ok, "deadlock"
