@@ -1851,7 +1851,17 @@ struct Consumer {
             vof[j] = kv_elem(0u, 0u, ts_log2, halves, 1, (16 * wc + (q >> 1) * 8 + (lane & 7)) & ((1 << ts_log2) - 1),
                              16 * j + (q & 1) * 8);
         }
-        const uint32_t qlane = qb + (uint32_t)(((lane & 7) * kQhlStride + ((lane >> 3) & 1) * 8) * 2);
+        // the queries' B-operand fragments are the same every step: held in registers
+        uint32_t qfr[8][2];
+        {
+            const uint32_t qlane = qb + (uint32_t)(((lane & 7) * kQhlStride + ((lane >> 3) & 1) * 8) * 2);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                if (ks < nks) ldsm_x2(qfr[ks], qlane + (uint32_t)(ks * 32));
+        }
+        // the softmax runs in base 2: scores times log2(e), so that each
+        // weight is one exp2; the running maxima are converted back at the end
+        constexpr float kLog2e = 1.4426950408889634f, kLn2 = 0.6931471805599453f;
         const uint64_t tb0 = tracing ? globaltimer_ns() : 0;
         for (int32_t blk = r.blo; blk < r.bhi; blk += 2) {
             const int NB = (blk + 1 < r.bhi) ? 2 : 1;
@@ -1867,10 +1877,9 @@ struct Consumer {
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     if (ks < nks) {
-                        uint32_t a[4], qf[2];
+                        uint32_t a[4];
                         ldsm_x4(a, sbw + kof[ks]);
-                        ldsm_x2(qf, qlane + (uint32_t)(ks * 32));
-                        mma_bf16_16816((ks & 1) ? sodd : sacc, a, qf);
+                        mma_bf16_16816((ks & 1) ? sodd : sacc, a, qfr[ks]);
                     }
                 }
 #pragma unroll
@@ -1883,7 +1892,7 @@ struct Consumer {
                     if (G == 1) v = (i & 1) ? 0.f : sacc[i] + sacc[i + 1];
                     else v += __shfl_xor_sync(0xFFFFFFFFu, v, partner);
                     const int tok = 16 * wc + tr + (i >> 1) * 8;
-                    sv[i] = (tok0 + tok < r.ctx) ? v : -INFINITY;
+                    sv[i] = (tok0 + tok < r.ctx) ? v * kLog2e : -INFINITY;
                 }
                 // the step's maximum per head over this warp's 16 tokens
                 float mx[2] = {fmaxf(sv[0], sv[2]), fmaxf(sv[1], sv[3])};
@@ -1896,12 +1905,12 @@ struct Consumer {
                 for (int j = 0; j < 2; ++j) {
                     nm[j] = fmaxf(wm[j], mx[j]);
                     alpha[j] = (nm[j] == -INFINITY || wm[j] == -INFINITY) ? (nm[j] == -INFINITY ? 1.f : 0.f)
-                                                                         : expf(wm[j] - nm[j]);
+                                                                         : exp2f(wm[j] - nm[j]);
                 }
                 float pv[4], ps[2] = {0.f, 0.f};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    pv[i] = (sv[i] == -INFINITY) ? 0.f : expf(sv[i] - nm[i & 1]);
+                    pv[i] = (sv[i] == -INFINITY) ? 0.f : exp2f(sv[i] - nm[i & 1]);
                     ps[i & 1] += pv[i];
                 }
 #pragma unroll
@@ -1924,12 +1933,15 @@ struct Consumer {
                 } else {
                     ca1 = alpha[0];  // G = 1: columns 0 and 1 are head 0's high and low parts
                 }
+                // (most steps leave every head's maximum where it was)
+                if (__any_sync(0xFFFFFFFFu, ca0 != 1.f || ca1 != 1.f)) {
 #pragma unroll
-                for (int mt = 0; mt < 8; ++mt) {
-                    o2[mt][0] *= ca0;
-                    o2[mt][1] *= ca1;
-                    o2[mt][2] *= ca0;
-                    o2[mt][3] *= ca1;
+                    for (int mt = 0; mt < 8; ++mt) {
+                        o2[mt][0] *= ca0;
+                        o2[mt][1] *= ca1;
+                        o2[mt][2] *= ca0;
+                        o2[mt][3] *= ca1;
+                    }
                 }
                 // the weights as the B operand P^T[16 tokens][2G columns]:
                 // high parts in the head lanes' columns, low parts in their
@@ -2016,8 +2028,8 @@ struct Consumer {
                     const int h = (G == 1) ? 0 : 2 * cq + j;
                     const float mb = mm[wc * 4 + h], lb = ml[wc * 4 + h];
                     const float M = fmaxf(wm[j], mb);
-                    const float wa = (wm[j] == -INFINITY) ? 0.f : expf(wm[j] - M);
-                    const float wb = (mb == -INFINITY) ? 0.f : expf(mb - M);
+                    const float wa = (wm[j] == -INFINITY) ? 0.f : exp2f(wm[j] - M);
+                    const float wb = (mb == -INFINITY) ? 0.f : exp2f(mb - M);
 #pragma unroll
                     for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
@@ -2041,12 +2053,12 @@ struct Consumer {
                     const int h = (G == 1) ? 0 : 2 * cq + (i & 1);
                     if (mt < nks && (G != 1 || (i & 1) == 0)) mo[(16 * mt + tr + (i >> 1) * 8) * 4 + h] = oh[mt][i];
                 }
-            if (tr == 0) {
+            if (tr == 0) {  // running maxima back in natural units
                 const int h0 = (G == 1) ? 0 : 2 * cq;
-                sc->att_m[h0] = wm[0];
+                sc->att_m[h0] = wm[0] * kLn2;
                 sc->att_l[h0] = wl[0];
                 if (G != 1) {
-                    sc->att_m[h0 + 1] = wm[1];
+                    sc->att_m[h0 + 1] = wm[1] * kLn2;
                     sc->att_l[h0 + 1] = wl[1];
                 }
             }
