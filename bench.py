@@ -55,14 +55,18 @@ def step_bytes(m, batch: int, ctx: int) -> int:
     return weight_bytes_read(m, batch) + batch * (per_tok * (ctx - 1) + per_tok + m.vocab * 4)
 
 
-# DRAM bytes (read + write) of one megakernel launch from an ncu capture of
-# the full-size workload (dram__bytes_read.sum + dram__bytes_write.sum, one
-# pass), keyed by (workload, batch) and by the fingerprint of the kernel
-# sources the capture ran.  A source change makes the entry stale and the
-# bench line reports null.
+# DRAM bytes (read + write) of one megakernel launch of the full-size
+# workload, from ncu captures (dram__bytes_read.sum + dram__bytes_write.sum,
+# one pass) of the same workload cut to 2 and 4 layers: the 4-layer launch
+# plus 28 times the per-layer difference (the rest of the launch, embedding
+# and LM head, is the same at every depth).  Keyed by (workload, batch) and by
+# the fingerprint of the kernel sources the captures ran; a source change
+# makes the entry stale and the bench line reports null.
 NCU_TRAFFIC = {
-    ("8b", 1): {"fingerprint": "b2c25ddf0e6f66d0", "bytes": 15.02e9 + 42.7e6,
+    ("8b", 1): {"fingerprint": "a98c0e28aa10939b", "bytes": 2.818347e9 + 28 * 0.440594e9,
                 "summary": "profiles/megakernel_8b_b1_dram.md"},
+    ("8b-batch", 64): {"fingerprint": "a98c0e28aa10939b", "bytes": 7.217662e9 + 28 * 1.539390e9,
+                       "summary": "profiles/megakernel_8b_b64_dram.md"},
 }
 
 
