@@ -137,7 +137,10 @@ typedef struct {
                               tile of a projection; small projections then run on fewer CTAs
                               with fewer partial sums to add (0: every CTA takes a range of
                               every projection) */
-    int32_t reserved[2];
+    int32_t tc_k_subtiles; /* tensor-core path: 64-column K sub-tiles per projection unit (ring
+                              slot), 1 or 2; two halve the waits and commits per weight byte
+                              but make slots twice as large (0: 2) */
+    int32_t reserved[1];
 } mk_plan_options;
 
 typedef struct mk_plan mk_plan; /* opaque, library-owned */

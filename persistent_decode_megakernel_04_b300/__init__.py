@@ -44,7 +44,8 @@ class mk_plan_options(ctypes.Structure):
                 ("timeout_ms", _i32), ("planner_seed", ctypes.c_uint32), ("l2_prefetch_kb", _i32),
                 ("test_unreachable_event", _i32), ("trace", _i32), ("tensor_cores", _i32), ("max_inflight", _i32),
                 ("kv_append", _i32), ("prefill_by_decode", _i32), ("jit", _i32),
-                ("test_poison_scratch", _i32), ("tc_tile_split", _i32), ("reserved", _i32 * 2)]
+                ("test_poison_scratch", _i32), ("tc_tile_split", _i32), ("tc_k_subtiles", _i32),
+                ("reserved", _i32 * 1)]
 
 
 class mk_device_error(ctypes.Structure):

@@ -594,6 +594,7 @@ mk_status mk_plan_create_ex(const mk_model_cfg *cfg, const mk_weight_ptrs *w, co
         k.h_tiles = g.h_tiles;
         k.aslot_bytes = g.aslot_bytes;
         k.num_aslots = g.num_aslots;
+        k.tc_sub = g.tc_sub;
         uint32_t cols = 32;
         while (cols < (uint32_t)(8 * g.npad)) cols <<= 1;  // two buffers x (gate, up) x 2 * npad columns
         k.tmem_cols = cols;

@@ -593,12 +593,14 @@ struct Producer {
         return true;
     }
 
-    // Batched path: one 128 x 64 weight tile per slot by TMA (two for
-    // gate/up: the gate tile, then the matching up tile).
+    // Batched path: one unit of 128 rows x tc_sub 64-column sub-tiles per
+    // slot by TMA, one copy per sub-tile (two units for gate/up: the gate
+    // tile, then the matching up tile).
     __device__ bool run_gemm(const Ctx &c, const Task &t) {
         const KParams &p = *c.p;
         const TcGeom &g = p.tcg[t.op];
         const int mats = (t.op == OP_GU) ? 2 : 1;
+        const int sub = p.tc_sub;
         for (int32_t u = t.a0; u < t.a1; ++u) {
             const int32_t tile = u / g.kchunks, kc = u % g.kchunks;
             for (int m = 0; m < mats; ++m) {
@@ -607,8 +609,9 @@ struct Producer {
                 int lt;
                 const int map = weight_map(p, t.op, t.layer, tile, m, &lt);
                 mbar_arrive_expect_tx(&c.sc->full[s], slot_bytes);
-                tma_load_2d(c.ring + (size_t)s * slot_bytes, tmap(p, map), kc * kTcTileK, lt * kTcTileM,
-                            &c.sc->full[s], pol);
+                for (int j = 0; j < sub; ++j)
+                    tma_load_2d(c.ring + (size_t)s * slot_bytes + (size_t)j * kTcTileM * kTcTileK * 2, tmap(p, map),
+                                (kc * sub + j) * kTcTileK, lt * kTcTileM, &c.sc->full[s], pol);
                 ++issued;
             }
         }
@@ -706,7 +709,9 @@ struct ActProducer {
             const uint32_t s = si;
             if (!wait_mbar(c, &c.sc->aempty[s], sph ^ 1u, SITE_EMPTY_WAIT)) return false;
             mbar_arrive_expect_tx(&c.sc->afull[s], (uint32_t)p.aslot_bytes);
-            tma_load_2d(c.aring + (size_t)s * p.aslot_bytes, map, kc * kTcTileK, 0, &c.sc->afull[s], pol);
+            for (int j = 0; j < p.tc_sub; ++j)
+                tma_load_2d(c.aring + (size_t)s * p.aslot_bytes + (size_t)j * (p.aslot_bytes / p.tc_sub), map,
+                            (kc * p.tc_sub + j) * kTcTileK, 0, &c.sc->afull[s], pol);
             ++issued;
             if (++si == ns) {
                 si = 0;
@@ -1457,6 +1462,10 @@ struct Consumer {
         const uint64_t wdesc0 = umma_desc_sw128(smem_u32(c.ring)), adesc0 = umma_desc_sw128(smem_u32(c.aring));
         const uint32_t wstep = slot_bytes >> 4, astep = (uint32_t)p.aslot_bytes >> 4;
         const uint32_t idesc = p.idesc, mstride = 2u * (uint32_t)p.npad;
+        const int sub = p.tc_sub;
+        // descriptor offset of sub-tile j: weights 128 x 64 bf16 = 16 KB apart,
+        // activations the slot's share
+        const uint32_t wsub = (uint32_t)(kTcTileM * kTcTileK * 2) >> 4, asub = ((uint32_t)p.aslot_bytes / sub) >> 4;
         uint32_t sg = seg;
         for (int32_t tile = t0; tile <= t1; ++tile, ++sg) {
             const int32_t klo = (tile == t0) ? t.a0 % g.kchunks : 0;
@@ -1494,10 +1503,11 @@ struct Consumer {
                 const uint64_t ad = adesc0 + (uint64_t)(as * astep);
                 for (int m = 0; m < mats; ++m) {
                     const uint64_t wd = wdesc0 + (uint64_t)(ws[m] * wstep);
+                    for (int j = 0; j < sub; ++j)
 #pragma unroll
-                    for (int kk = 0; kk < kTcTileK / 16; ++kk)  // K = 16 bf16 = 32 bytes = 2 descriptor units
-                        umma_bf16(dcol + (uint32_t)m * mstride, wd + 2u * kk, ad + 2u * kk, idesc,
-                                  (k > klo || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < kTcTileK / 16; ++kk)  // K = 16 bf16 = 32 bytes = 2 descriptor units
+                            umma_bf16(dcol + (uint32_t)m * mstride, wd + j * wsub + 2u * kk, ad + j * asub + 2u * kk,
+                                      idesc, (k > klo || j > 0 || kk > 0) ? 1u : 0u);
                 }
                 for (int m = 0; m < mats; ++m) umma_commit(&sc->empty[ws[m]]);
                 umma_commit(&sc->aempty[as]);

@@ -94,6 +94,7 @@ struct KParams {
     int32_t num_ctas;        // ranges per projection
     int32_t h_tiles;         // 128-row tiles of the hidden size
     int32_t aslot_bytes, num_aslots;
+    int32_t tc_sub;  // 64-column K sub-tiles per projection unit (one ring slot, one activation slot)
     uint32_t tmem_cols;
     TcGeom tcg[OP_COUNT];
     const uint8_t *tmaps;    // CUtensorMap[7 * L + 4], see the kernel's TmIdx

@@ -97,12 +97,12 @@ mk_plan_options resolve_options(const mk_model_cfg &cfg, const mk_plan_options *
 
 namespace {
 
-TcGeom make_tc_geom(int32_t K, int32_t rows, int32_t ctr_off) {
+TcGeom make_tc_geom(int32_t K, int32_t rows, int32_t ctr_off, int32_t sub) {
     TcGeom t{};
     t.K = K;
     t.rows = rows;
     t.tiles = (rows + kTcTileM - 1) / kTcTileM;
-    t.kchunks = (K + kTcTileK - 1) / kTcTileK;
+    t.kchunks = (K + kTcTileK * sub - 1) / (kTcTileK * sub);  // units of sub 64-column sub-tiles
     t.units = t.tiles * t.kchunks;
     t.ctr_off = ctr_off;
     return t;
@@ -127,7 +127,11 @@ mk_status build_plan(const mk_model_cfg &cfg, const mk_plan_options &opt, PlanTa
     g.tc = tc;
     g.num_ctas = N;
     g.attn_splits = S;
-    g.slot_bytes = tc ? kTcTileM * kTcTileK * 2 : opt.slot_bytes;
+    if (opt.tc_k_subtiles < 0 || opt.tc_k_subtiles > 2) return MK_ERR_INVALID;
+    // two sub-tiles measured faster at batch 8, 32 and 64 (half the MMA
+    // warp's waits and commits per weight byte outweigh the shallower ring)
+    if (tc) g.tc_sub = opt.tc_k_subtiles > 0 ? opt.tc_k_subtiles : 2;
+    g.slot_bytes = tc ? kTcTileM * kTcTileK * 2 * g.tc_sub : opt.slot_bytes;
     g.num_slots = opt.num_slots;
     // KV tokens per ring slot: a 64-token attention block fills 1 or 2 slots
     g.tps = (g.slot_bytes >= 2 * d * 2 * 64) ? 64 : 32;
@@ -149,24 +153,25 @@ mk_status build_plan(const mk_model_cfg &cfg, const mk_plan_options &opt, PlanTa
     } else {
         g.npad = (B + 15) / 16 * 16;
         // activation tiles hold 2 * npad rows: the bf16 high parts, then the bf16 low parts
-        g.aslot_bytes = 2 * g.npad * kTcTileK * 2;
+        g.aslot_bytes = 2 * g.npad * kTcTileK * 2 * g.tc_sub;
         g.num_aslots = std::max(2, std::min(8, (48 * 1024) / g.aslot_bytes));
         g.h_tiles = (H + kTcTileM - 1) / kTcTileM;
         int32_t ctr = 0;
         const int32_t tq = (nq * d + kTcTileM - 1) / kTcTileM, tk = (nkv * d + kTcTileM - 1) / kTcTileM;
-        g.tcg[OP_QKV] = make_tc_geom(H, (nq + 2 * nkv) * d, ctr);
+        const int32_t sub = g.tc_sub;
+        g.tcg[OP_QKV] = make_tc_geom(H, (nq + 2 * nkv) * d, ctr, sub);
         g.tcg[OP_QKV].tiles = tq + 2 * tk;  // q, k and v tiled separately
         g.tcg[OP_QKV].units = g.tcg[OP_QKV].tiles * g.tcg[OP_QKV].kchunks;
         g.tcg[OP_QKV].tiles_q = tq;
         g.tcg[OP_QKV].tiles_k = tk;
         ctr += g.tcg[OP_QKV].tiles;
-        g.tcg[OP_O] = make_tc_geom(nq * d, H, ctr);
+        g.tcg[OP_O] = make_tc_geom(nq * d, H, ctr, sub);
         ctr += g.tcg[OP_O].tiles;
-        g.tcg[OP_GU] = make_tc_geom(H, I, ctr);
+        g.tcg[OP_GU] = make_tc_geom(H, I, ctr, sub);
         ctr += g.tcg[OP_GU].tiles;
-        g.tcg[OP_DOWN] = make_tc_geom(I, H, ctr);
+        g.tcg[OP_DOWN] = make_tc_geom(I, H, ctr, sub);
         ctr += g.tcg[OP_DOWN].tiles;
-        g.tcg[OP_LM] = make_tc_geom(H, V, ctr);
+        g.tcg[OP_LM] = make_tc_geom(H, V, ctr, sub);
         ctr += g.tcg[OP_LM].tiles;
         // ranges per projection: every CTA, or at most tc_tile_split per row tile
         for (int op : {OP_QKV, OP_O, OP_GU, OP_DOWN, OP_LM}) {

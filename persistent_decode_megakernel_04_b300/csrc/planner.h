@@ -23,6 +23,7 @@ struct PlanGeom {
     // batched (tensor-core) path
     bool tc = false;
     int32_t npad = 0;         // batch rounded up to the MMA N granule (16)
+    int32_t tc_sub = 1;       // 64-column K sub-tiles per projection unit (ring slot)
     int32_t aslot_bytes = 0;  // activation ring slot: npad rows x 64 bf16
     int32_t num_aslots = 0;
     int32_t h_tiles = 0;      // 128-row tiles of the hidden size

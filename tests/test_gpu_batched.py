@@ -235,3 +235,16 @@ def test_tiny_batched_dynamic_dispatch(cuda_device):
     plan, kv = harness.gpu_plan(TINY, max_seq, batch=8, opts=mk.mk_plan_options(jit=1))
     model = harness.oracle_model(TINY)
     harness.run_teacher_forced_batch(plan, kv, model, prompts(8, 40, seed=6), 4, max_seq, rows=[0, 3, 7])
+
+
+@pytest.mark.parametrize("B,sub", [(8, 1), (64, 1), (24, 2)], ids=["b8-sub1", "b64-sub1", "b24-sub2"])
+def test_tiny_batched_k_subtiles(cuda_device, B, sub):
+    """Projection units of one or two 64-column K sub-tiles (tc_k_subtiles),
+    against the default for the batch; the tiny decoder's FFN width 688 is
+    not a multiple of 128, so the last unit's second sub-tile reads past K
+    (zero-filled on both operands)."""
+    max_seq = 128
+    plan, kv = harness.gpu_plan(TINY, max_seq, batch=B, opts=mk.mk_plan_options(tc_k_subtiles=sub))
+    model = harness.oracle_model(TINY)
+    harness.run_teacher_forced_batch(plan, kv, model, prompts(B, 20, seed=11), 4, max_seq, rows=[0, B - 1],
+                                     ablation_every=2)

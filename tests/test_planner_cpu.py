@@ -147,8 +147,13 @@ def describe_b(name, B, num_ctas, **kw):
     return m, tasks, n_events
 
 
-def tc_units(m, op):
-    T, K = mk.TC_TILE_M, mk.TC_TILE_K
+def tc_sub_default(B):
+    """64-column K sub-tiles per projection unit by default."""
+    return 2
+
+
+def tc_units(m, op, B=64):
+    T, K = mk.TC_TILE_M, mk.TC_TILE_K * tc_sub_default(B)
     cdiv = lambda a, b: (a + b - 1) // b
     d = m.head_dim
     if op == mk.OP_QKV:
@@ -169,7 +174,7 @@ def test_batched_units_covered_once_and_balanced(name, B, num_ctas):
             cover[(t.layer, t.op)].append((t.a0, t.a1, t.a2))
     for l in range(m.n_layers):
         for op in (mk.OP_QKV, mk.OP_O, mk.OP_GU, mk.OP_DOWN):
-            U, _ = tc_units(m, op)
+            U, _ = tc_units(m, op, B)
             rs = sorted(cover[(l, op)])
             assert rs[0][0] == 0 and rs[-1][1] == U
             assert all(a[1] == b[0] for a, b in zip(rs, rs[1:])), "gap or overlap"
@@ -349,8 +354,9 @@ def test_tile_split_bounds_the_ranges_per_row_tile(split):
     tasks, n_events = mk.mk_plan_describe(cfg, N, mk.mk_plan_options(tc_tile_split=split))
     H, I, V, d = m.hidden, m.ffn_dim, m.vocab, m.head_dim
     qkv_tiles = (m.n_q_heads * d + 127) // 128 + 2 * ((m.n_kv_heads * d + 127) // 128)
-    geo = {mk.OP_QKV: (qkv_tiles, H // 64), mk.OP_O: (H // 128, m.n_q_heads * d // 64),
-           mk.OP_GU: (I // 128, H // 64), mk.OP_DOWN: (H // 128, I // 64), mk.OP_LM: ((V + 127) // 128, H // 64)}
+    kw = 64 * tc_sub_default(B)  # K columns per unit
+    geo = {mk.OP_QKV: (qkv_tiles, H // kw), mk.OP_O: (H // 128, m.n_q_heads * d // kw),
+           mk.OP_GU: (I // 128, H // kw), mk.OP_DOWN: (H // 128, I // kw), mk.OP_LM: ((V + 127) // 128, H // kw)}
     for op, (tiles, kchunks) in geo.items():
         ts = sorted((t for t in tasks if t.op == op and t.layer == (m.n_layers - 1 if op == mk.OP_LM else 3)),
                     key=lambda t: t.a0)
@@ -369,3 +375,18 @@ def test_tile_split_bounds_the_ranges_per_row_tile(split):
         assert min(o, key=lambda t: t.a2).cta == n_att % N
     ok, _, _ = simulate(m, tasks, n_events)
     assert ok, "deadlock"
+
+
+@pytest.mark.parametrize("B,sub", [(8, 1), (8, 2), (64, 1), (64, 2)])
+def test_k_subtiles_set_the_unit_width(B, sub):
+    """tc_k_subtiles: a projection unit spans sub 64-column K sub-tiles, so
+    each operator has tiles * ceil(K / (64 sub)) units, covered once."""
+    m = SHAPES["8b"]
+    cfg = mk.model_cfg(m, B, 1024)
+    tasks, _ = mk.mk_plan_describe(cfg, 148, mk.mk_plan_options(tc_k_subtiles=sub))
+    cdiv = lambda a, b: (a + b - 1) // b
+    for op, (rows, K) in {mk.OP_O: (m.hidden, m.n_q_heads * m.head_dim), mk.OP_DOWN: (m.hidden, m.ffn_dim),
+                          mk.OP_GU: (m.ffn_dim, m.hidden)}.items():
+        rs = sorted((t.a0, t.a1) for t in tasks if t.op == op and t.layer == 0)
+        assert rs[0][0] == 0 and rs[-1][1] == cdiv(rows, 128) * cdiv(K, 64 * sub)
+        assert all(a[1] == b[0] for a, b in zip(rs, rs[1:]))
