@@ -63,9 +63,9 @@ def step_bytes(m, batch: int, ctx: int) -> int:
 # the fingerprint of the kernel sources the captures ran; a source change
 # makes the entry stale and the bench line reports null.
 NCU_TRAFFIC = {
-    ("8b", 1): {"fingerprint": "a98c0e28aa10939b", "bytes": 2.818347e9 + 28 * 0.440594e9,
+    ("8b", 1): {"fingerprint": "9c2ef2ebc55bacef", "bytes": 2.818887e9 + 28 * 0.441081e9,
                 "summary": "profiles/megakernel_8b_b1_dram.md"},
-    ("8b-batch", 64): {"fingerprint": "a98c0e28aa10939b", "bytes": 7.217662e9 + 28 * 1.539390e9,
+    ("8b-batch", 64): {"fingerprint": "9c2ef2ebc55bacef", "bytes": 7.192775e9 + 28 * 1.534003e9,
                        "summary": "profiles/megakernel_8b_b64_dram.md"},
 }
 
