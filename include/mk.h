@@ -100,7 +100,10 @@ typedef struct {
 typedef struct {
     int32_t num_ctas;      /* worker CTAs (default: every SM) */
     int32_t attn_splits;   /* context splits per (sequence, kv head), at most 64
-                              (default: CTAs / (batch*n_kv_heads), capped at 64) */
+                              (default: CTAs / (batch*n_kv_heads), capped at 64).  With one
+                              split and more pairs than CTAs, the pairs left over after whole
+                              rounds of CTAs are cut into the split count that evens the
+                              CTAs' shares (static dispatch) */
     int32_t slot_bytes;    /* shared-memory ring slot size (default 32768) */
     int32_t num_slots;     /* ring slots (default 6 at batch 1; batched: as many as shared memory holds) */
     int32_t timeout_ms;    /* budget of every device wait (default 2000) */

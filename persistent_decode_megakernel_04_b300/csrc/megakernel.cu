@@ -2380,7 +2380,8 @@ struct Consumer {
             return;
         }
         // partial result of this split: unnormalised o (high + low columns), running max, sum
-        const int64_t pidx = (((int64_t)b * p.nkv + kvh) * S + t.a2) * G;
+        // partial sums of pair (b, kvh) at a stride of the plan's largest split count
+        const int64_t pidx = (((int64_t)b * p.nkv + kvh) * p.attn_splits + t.a2) * G;
         if (wc < nks) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -2413,7 +2414,7 @@ struct Consumer {
             // one round trip), then every thread sums its output pairs over
             // the splits, eight loads in flight at a time.
             if (ct == 0) *done = 0u;  // nothing else touches it in this launch
-            const int64_t pbase = ((int64_t)b * p.nkv + kvh) * S * G;
+            const int64_t pbase = ((int64_t)b * p.nkv + kvh) * p.attn_splits * G;
             if (wc < G) {
                 const int g = wc;
                 float M = -INFINITY;

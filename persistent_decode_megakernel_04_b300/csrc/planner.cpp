@@ -120,7 +120,33 @@ mk_status build_plan(const mk_model_cfg &cfg, const mk_plan_options &opt, PlanTa
         opt.attn_splits > kMaxSplits || (tc ? (opt.num_slots == 1 || opt.num_slots < 0) : opt.num_slots < 2))
         return MK_ERR_INVALID;
     const int32_t H = cfg.hidden, d = cfg.head_dim, nq = cfg.n_q_heads, nkv = cfg.n_kv_heads;
-    const int32_t I = cfg.ffn_dim, V = cfg.vocab, L = cfg.n_layers, B = cfg.batch, S = opt.attn_splits;
+    const int32_t I = cfg.ffn_dim, V = cfg.vocab, L = cfg.n_layers, B = cfg.batch;
+    // Context splits of each (sequence, kv head) pair.  With more pairs than
+    // CTAs and one split asked for (the default there), the pairs left over
+    // after whole rounds of CTAs are cut into k splits, k (at most 8) chosen
+    // to minimise the last round's length: ceil(R k / N) tasks of 1/k of a
+    // pair's work plus a fixed cost per task (setup, partial, merge) taken
+    // as 0.12 of a pair's.  Batch 64 of 8 kv heads on 148 CTAs: 444 whole
+    // pairs, 68 pairs in halves, 3.5 pairs' work on the busiest CTA, not 4.
+    const int32_t P = B * nkv;
+    std::vector<int32_t> psplit(P, opt.attn_splits);
+    if (opt.attn_splits == 1 && P > N && !opt.jit) {
+        const int32_t R = P % N;
+        if (R > 0) {
+            constexpr double kTaskCost = 0.12;
+            int32_t best_k = 1;
+            double best = 1.0 + kTaskCost;
+            for (int32_t k = 2; k <= 8; ++k) {
+                const double t = (double)((R * k + N - 1) / N) * (1.0 / k + kTaskCost);
+                if (t < best * 0.98) {
+                    best = t;
+                    best_k = k;
+                }
+            }
+            for (int32_t i = P - R; i < P; ++i) psplit[i] = best_k;
+        }
+    }
+    const int32_t S = *std::max_element(psplit.begin(), psplit.end());  // partial-sum stride per pair
 
     PlanGeom &g = out->g;
     g = PlanGeom{};
@@ -271,12 +297,14 @@ mk_status build_plan(const mk_model_cfg &cfg, const mk_plan_options &opt, PlanTa
             att_cnt = emit_ranges(OP_KVA, l, B * nkv, ev(l, OP_QKV), n_qkv, ev(l, OP_KVA));
             att_ev = ev(l, OP_KVA);
         }
-        // attention: one task per (sequence, kv head, split), round-robin over CTAs
+        // attention: one task per (sequence, kv head, split), round-robin over
+        // CTAs in pair order (the pairs cut into more splits come last)
         begin_stage();
         int32_t i = 0;
         for (int32_t b = 0; b < B; ++b)
-            for (int32_t h = 0; h < nkv; ++h)
-                for (int32_t s = 0; s < S; ++s, ++i) {
+            for (int32_t h = 0; h < nkv; ++h) {
+                const int32_t sp = psplit[b * nkv + h];
+                for (int32_t s = 0; s < sp; ++s, ++i) {
                     Task t{};
                     t.op = OP_ATTN;
                     t.layer = (uint16_t)l;
@@ -286,9 +314,10 @@ mk_status build_plan(const mk_model_cfg &cfg, const mk_plan_options &opt, PlanTa
                     t.a0 = b;
                     t.a1 = h;
                     t.a2 = s;
-                    t.a3 = S;
+                    t.a3 = sp;
                     push(t, i);
                 }
+            }
         cursor = i % N;
         emit_ranges(OP_O, l, items(OP_O), ev(l, OP_ATTN), (uint32_t)(B * nkv), ev(l, OP_O));
         emit_ranges(OP_GU, l, items(OP_GU), ev(l, OP_O), n_o, ev(l, OP_GU));

@@ -40,8 +40,8 @@ def test_tiny_batched_random_gains_and_ablation(cuda_device):
 @pytest.mark.parametrize("opts", [dict(num_ctas=7, attn_splits=3, planner_seed=5),
                                   dict(num_ctas=148, attn_splits=1, num_slots=3, planner_seed=9),
                                   dict(num_ctas=1), dict(tc_tile_split=1), dict(tc_tile_split=2, planner_seed=3),
-                                  dict(tc_tile_split=3, num_ctas=20)],
-                         ids=["7ctas", "3slots", "1cta", "split1", "split2", "split3-20ctas"])
+                                  dict(tc_tile_split=3, num_ctas=20), dict(num_ctas=5)],
+                         ids=["7ctas", "3slots", "1cta", "split1", "split2", "split3-20ctas", "5ctas-balanced-splits"])
 def test_tiny_batched_schedules(cuda_device, opts):
     # row tiles shared by several ranges (fixup), a permuted CTA assignment,
     # a shallow weight ring and a single worker CTA

@@ -390,3 +390,36 @@ def test_k_subtiles_set_the_unit_width(B, sub):
         rs = sorted((t.a0, t.a1) for t in tasks if t.op == op and t.layer == 0)
         assert rs[0][0] == 0 and rs[-1][1] == cdiv(rows, 128) * cdiv(K, 64 * sub)
         assert all(a[1] == b[0] for a, b in zip(rs, rs[1:]))
+
+
+@pytest.mark.parametrize("B,N", [(64, 148), (32, 148), (16, 37), (20, 148)])
+def test_leftover_attention_pairs_are_split_to_even_the_ctas(B, N):
+    """With more (sequence, kv head) pairs than CTAs and the default single
+    split, the pairs left over after whole rounds are cut into k splits: every
+    pair is covered by its splits exactly once, and no CTA carries more than
+    the even share rounded up to 1/k of a pair (a whole extra pair before)."""
+    m = SHAPES["8b"]
+    cfg = mk.model_cfg(m, B, 4160)
+    tasks, n_events = mk.mk_plan_describe(cfg, N, mk.mk_plan_options(num_ctas=N))
+    att = [t for t in tasks if t.op == mk.OP_ATTN and t.layer == 0]
+    P = B * m.n_kv_heads
+    pairs = defaultdict(list)
+    for t in att:
+        pairs[(t.a0, t.a1)].append((t.a2, t.a3))
+    assert len(pairs) == P
+    for sp in pairs.values():
+        k = sp[0][1]
+        assert sorted(s for s, _ in sp) == list(range(k)) and all(kk == k for _, kk in sp)
+    load = defaultdict(float)
+    for t in att:
+        load[t.cta] += 1.0 / t.a3
+    R = P % N
+    ks = {sp[0][1] for sp in pairs.values()}
+    if P > N and R:
+        k = max(ks)
+        assert ks <= {1, k} and k <= 8
+        assert max(load.values()) <= P // N + (-(-R * k // N)) / k + 1e-9
+    if (B, N) == (64, 148):
+        assert ks == {1, 2} and max(load.values()) == 3.5  # 444 whole pairs, 68 in halves
+    ok, _, _ = simulate(m, tasks, n_events)
+    assert ok, "deadlock"
