@@ -63,9 +63,9 @@ def step_bytes(m, batch: int, ctx: int) -> int:
 # the fingerprint of the kernel sources the captures ran; a source change
 # makes the entry stale and the bench line reports null.
 NCU_TRAFFIC = {
-    ("8b", 1): {"fingerprint": "9c2ef2ebc55bacef", "bytes": 2.818887e9 + 28 * 0.441081e9,
+    ("8b", 1): {"fingerprint": "f85a1c652a69deed", "bytes": 2.818927e9 + 28 * 0.440913e9,
                 "summary": "profiles/megakernel_8b_b1_dram.md"},
-    ("8b-batch", 64): {"fingerprint": "9c2ef2ebc55bacef", "bytes": 7.192775e9 + 28 * 1.534003e9,
+    ("8b-batch", 64): {"fingerprint": "f85a1c652a69deed", "bytes": 7.195817e9 + 28 * 1.535045e9,
                        "summary": "profiles/megakernel_8b_b64_dram.md"},
 }
 
