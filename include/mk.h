@@ -272,8 +272,10 @@ mk_status mk_decode_step_greedy_host(mk_plan *plan, const int32_t *tokens_host, 
  *   k=6 (batched projections) total time the MMA issuer waited for
  *       activation tiles, k=7 ... for a free TMEM accumulator.
  * On the batched path k=3 of a projection task is the MMA issuer's wait for
- * weight tiles.  For attention tasks k=6 is the time spent in slot waits and
- * scores, k=7 the time in value sums (the rest is softmax and per-task work).
+ * weight tiles (the MMA warp's).  For attention tasks k=6 is the time spent
+ * in slot waits and scores, k=7 the time in value sums (the rest is softmax
+ * and per-task work); on the warp-local path of long splits k=6 is the whole
+ * loop and k=3 the first compute warp's waits for its own slots.
  * Zeros mark tasks not run.  Synchronises `stream`.  Host buffer of
  * `capacity` uint64 values; MK_ERR_INVALID if tracing is off or the buffer is
  * too small (*max_tasks is still set). */
