@@ -72,3 +72,28 @@ def test_unsupported_shapes_are_reported():
 
 def test_null_step_arguments_rejected():
     assert mk.lib().mk_decode_step(None, None, None, None, None, None) == mk.MK_ERR_INVALID
+    for fn in ("mk_decode_step_greedy", "mk_decode_step_host", "mk_decode_step_greedy_host",
+               "mk_decode_step_ablation"):
+        assert getattr(mk.lib(), fn)(None, None, None, None, None, None) == mk.MK_ERR_INVALID, fn
+    assert mk.lib().mk_prefill(None, None, 4, None, None, None) == mk.MK_ERR_INVALID
+    assert mk.lib().mk_prefill_row(None, 0, None, 4, None, None, None) == mk.MK_ERR_INVALID
+    assert mk.lib().mk_greedy_next(None, None, None, None, None) == mk.MK_ERR_INVALID
+
+
+def test_plan_options_layout_matches_the_header():
+    """The binding's options struct has the header's fields in order (the
+    header's field names, read from mk.h, against the ctypes fields)."""
+    text = (ROOT / "include" / "mk.h").read_text()
+    body = text[text.index("typedef struct {\n    int32_t num_ctas;"):text.index("} mk_plan_options;")]
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    names = re.findall(r"\b(?:int32_t|uint32_t)\s+(\w+)", body)
+    assert [n for n, _ in mk.mk_plan_options._fields_] == names
+    assert ctypes.sizeof(mk.mk_plan_options) == 4 * (len(names) - 1 + 1)  # reserved[1] is one word
+
+
+@pytest.mark.parametrize("bad", [dict(tc_k_subtiles=3), dict(tc_k_subtiles=-1), dict(num_slots=1), dict(jit=17)])
+def test_out_of_range_options_rejected_on_host(bad):
+    c = mk.model_cfg(synth.WORKLOADS["tiny"].model, 8, 64)
+    with pytest.raises(mk.MKError) as e:
+        mk.mk_plan_describe(c, 148, mk.mk_plan_options(**bad))
+    assert e.value.status == mk.MK_ERR_INVALID
