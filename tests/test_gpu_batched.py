@@ -248,3 +248,18 @@ def test_tiny_batched_k_subtiles(cuda_device, B, sub):
     model = harness.oracle_model(TINY)
     harness.run_teacher_forced_batch(plan, kv, model, prompts(B, 20, seed=11), 4, max_seq, rows=[0, B - 1],
                                      ablation_every=2)
+
+
+@pytest.mark.parametrize("B,opts", [(64, {}), (8, dict(jit=1)), (1, {}), (40, dict(num_ctas=37))],
+                         ids=["b64", "b8-jit", "b1", "b40-37ctas"])
+def test_long_runs_with_poisoned_scratch(cuda_device, B, opts):
+    """150 teacher-forced steps with every activation buffer NaN-filled
+    before each step: a read racing ahead of its producer, or a ring slot
+    reused a round early, would show as a parity failure somewhere along the
+    run (the contexts grow across three 64-token pages)."""
+    max_seq = 256
+    plan, kv = harness.gpu_plan(TINY, max_seq, batch=B,
+                                opts=mk.mk_plan_options(test_poison_scratch=1, **opts))
+    model = harness.oracle_model(TINY)
+    harness.run_teacher_forced_batch(plan, kv, model, prompts(B, 20, seed=7), 150, max_seq, rows=sorted({0, B - 1}),
+                                     ablation_every=0 if opts.get("jit") else 50)
