@@ -180,7 +180,9 @@ mk_status build_plan(const mk_model_cfg &cfg, const mk_plan_options &opt, PlanTa
         g.npad = (B + 15) / 16 * 16;
         // activation tiles hold 2 * npad rows: the bf16 high parts, then the bf16 low parts
         g.aslot_bytes = 2 * g.npad * kTcTileK * 2 * g.tc_sub;
-        g.num_aslots = std::max(2, std::min(8, (48 * 1024) / g.aslot_bytes));
+        // 40 KB of activation slots: one more 32 KB weight slot fits at batch
+        // 8 to 32 (measured 1.4-2% faster than 48 KB), batch 64 keeps two
+        g.num_aslots = std::max(2, std::min(8, (40 * 1024) / g.aslot_bytes));
         g.h_tiles = (H + kTcTileM - 1) / kTcTileM;
         int32_t ctr = 0;
         const int32_t tq = (nq * d + kTcTileM - 1) / kTcTileM, tk = (nkv * d + kTcTileM - 1) / kTcTileM;
