@@ -117,7 +117,7 @@ typedef struct {
     int32_t trace;         /* nonzero: record per-task timestamps (see mk_plan_trace) */
     int32_t tensor_cores;  /* 0: projections as CUDA-core matvecs at batch 1, tcgen05 tiles at
                               batch >= 2; 1: tcgen05 tiles at every batch */
-    int32_t max_inflight;  /* ring copies a CTA keeps in flight at once (default: 2 at batch 1,
+    int32_t max_inflight;  /* ring copies a CTA keeps in flight at once (default: 3 at batch 1,
                               every free ring slot when batched; >= num_slots: no cap) */
     int32_t kv_append;     /* 1: a task of its own (op 8) RoPEs and appends every row's new K/V
                               to the cache before attention, which then reads the new token from
